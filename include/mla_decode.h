@@ -1,0 +1,213 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) MLA decode library
+ * (libmla_decode.so).
+ *
+ * The operation (kernelbot amd-mixed-mla submission 689529 "MLA decode V3",
+ * module constants and custom_kernel): single-token decode of DeepSeek-style
+ * Multi-head Latent Attention. 16 query heads share one KV head; a KV row is
+ * 576 values (512-wide latent + 64-wide rope part); for sequence b and head h
+ *   s_t      = sm_scale * <q[b,h,:], kv[row_t,:]>            (all 576 dims)
+ *   out[b,h] = sum_t softmax_t(s) * kv[row_t, 0:512]          (first 512 dims)
+ * with row_t = kv_indices[kv_indptr[b] + t] for 0 <= t < kv_indptr[b+1] -
+ * kv_indptr[b] (page_size = 1: every page is one row). The pages' V6c and
+ * v86 submissions run it as a persistent stage-1 kernel over a precomputed
+ * work list followed by a split reduce (submission 690201 "V6c",
+ * custom_kernel: direct stage1 and reduce calls; _build_cache: metadata and
+ * cached partial buffers); this library keeps that split: a host planner
+ * (mla_decode_plan) and a device pass (mla_decode = stage 1 + reduce).
+ *
+ * Conventions for every entry point:
+ *  - Return value: MLA_OK (0) or a negative mla_status. No C++ exception
+ *    crosses this boundary. mla_strerror() names a status.
+ *  - "device" pointers are CUDA global memory of the current device, owned
+ *    by the caller unless stated; "host" pointers are ordinary host memory.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Device work is asynchronous on that stream; nothing here synchronises
+ *    the stream except mla_plan_check_error().
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Problem constants fixed by the pages (V3 module constants). */
+#define MLA_NUM_HEADS 16
+#define MLA_NUM_KV_HEADS 1
+#define MLA_QK_HEAD_DIM 576
+#define MLA_V_HEAD_DIM 512
+#define MLA_PAGE_SIZE 1
+
+/* Value modes (dtype_mode argument). */
+enum mla_dtype_mode {
+  /* q bf16 [B,16,576], kv bf16 [slots,576]; kv_scale ignored. The pages'
+     non-persistent bf16 path (submission 641982 "v86", custom_kernel). */
+  MLA_MODE_BF16 = 0,
+  /* q bf16 [B,16,576] is cast inside the kernel to OCP fp8 e4m3fn with scale 1
+     (round to nearest even; magnitudes above 448 saturate) — the direct cast of
+     V3 / V6c custom_kernel; kv holds e4m3fn bytes [slots,576] with one fp32
+     per-tensor dequantisation scale *kv_scale (kv_data["fp8"] = (buffer,
+     scale)). Scores use q8 . k8 * sm_scale * kv_scale; out is scaled by
+     kv_scale. */
+  MLA_MODE_FP8 = 1
+};
+
+/* Status codes. */
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_ARG = -1,           /* null pointer, negative size, bad batch or num_sms */
+  MLA_ERR_DTYPE = -2,         /* unknown dtype_mode */
+  MLA_ERR_PLAN_MISMATCH = -3, /* device kv_indptr disagrees with the plan (reported by the kernel) */
+  MLA_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+  MLA_ERR_TIMEOUT = -5,       /* a bounded wait inside a kernel gave up (kernel returned early) */
+  MLA_ERR_ALIGN = -6,         /* q, kv or out not 16-byte aligned */
+  MLA_ERR_NOMEM = -7,         /* device or host allocation failed while planning */
+  MLA_ERR_INDEX = -8,         /* a kv_indices entry lies outside [0, num_kv_slots) (reported by the kernel) */
+  MLA_ERR_DEVICE = -9,        /* no usable sm_103 device, or the plan belongs to another device */
+  MLA_ERR_INDPTR = -10        /* host kv_indptr not non-decreasing from 0, or a sequence too long */
+};
+
+/* Opaque plan: split-KV work list, reduce map and the partial-result
+   workspace for one (batch, kv_indptr, num_sms) shape. Owned by the library. */
+typedef struct mla_plan mla_plan;
+
+/* Planner tunables (mla_decode_plan_ex). Zero in a field selects its default. */
+typedef struct mla_plan_options {
+  int64_t num_kv_slots;   /* rows in the KV pool; kv_indices are checked against it in the
+                             kernel (out-of-range rows are skipped and MLA_ERR_INDEX recorded).
+                             0 = unchecked (the plain mla_decode_plan) */
+  int min_rows_per_split; /* smallest KV chunk the planner cuts (default 256) */
+  int granularity;        /* chunk boundaries are multiples of this many rows (default 16) */
+  int ctas_per_sm;        /* persistent CTAs per SM (default 1) */
+} mla_plan_options;
+
+/* Read-only description of a plan. */
+typedef struct mla_plan_info {
+  int batch;
+  int num_ctas;           /* stage-1 grid size (persistent CTAs that received work) */
+  int num_work_items;     /* (sequence, KV chunk) items in the work list */
+  int num_partial_slots;  /* partial (O, LSE) slots in the workspace */
+  int num_split_seqs;     /* sequences whose chunks are merged by the reduce kernel */
+  int device;             /* CUDA device the plan's buffers live on */
+  int64_t total_rows;     /* sum of the sequence lengths */
+  int64_t max_rows_per_cta;
+  size_t workspace_bytes; /* device bytes the plan owns */
+} mla_plan_info;
+
+/*
+ * mla_decode_plan — host split-KV planner (the persistent-mode metadata of the
+ * pages: get_mla_metadata_info_v1 / get_mla_metadata_v1 in submission 598454
+ * "v12", _get_or_compute_metadata, and the cached logits / attn_lse buffers of
+ * 690201 "V6c", _build_cache).
+ *   batch          number of sequences B (>= 0).
+ *   kv_indptr_host host int32 [B+1]: kv_indptr[0] = 0, non-decreasing; sequence b
+ *                  owns kv_indices[kv_indptr[b] .. kv_indptr[b+1]). Read only
+ *                  during the call.
+ *   num_sms        SMs to spread the work over (<= 0: query the current device).
+ *   plan_out       receives the plan. Plans are cached by (device, batch,
+ *                  kv_indptr contents, num_sms, options): an identical request
+ *                  returns the same plan with its reference count raised.
+ * Allocates device memory (work list, reduce map, fp32 partial O [slots,16,512]
+ * and LSE [slots,16], an error word) on the current device; synchronises the
+ * device once to upload the work list. Errors: MLA_ERR_ARG, MLA_ERR_INDPTR,
+ * MLA_ERR_NOMEM, MLA_ERR_CUDA, MLA_ERR_DEVICE.
+ */
+int mla_decode_plan(int batch, const int32_t* kv_indptr_host, int num_sms, mla_plan** plan_out);
+
+/* mla_decode_plan with tunables (options may be NULL = defaults). */
+int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
+                       mla_plan** plan_out);
+
+/* Drop one reference to a plan; the last reference frees its device memory.
+   The caller must ensure no decode using the plan is still in flight. */
+int mla_plan_release(mla_plan* plan);
+
+/* Fill *info with the plan's shape. */
+int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info);
+
+/*
+ * mla_decode — one decode call: stage 1 (+ reduce when any sequence is split).
+ *   q          device bf16 [B,16,576], row-major, 16-byte aligned.
+ *   kv         device [num_slots,576] row-major: bf16 (MLA_MODE_BF16) or e4m3fn
+ *              bytes (MLA_MODE_FP8); 16-byte aligned.
+ *   kv_scale   device fp32 [1]: fp8 dequantisation scale (ignored in bf16 mode,
+ *              may then be NULL).
+ *   kv_indptr  device int32 [B+1], equal to the host array the plan was built
+ *              from (the kernel checks each sequence length it touches and
+ *              records MLA_ERR_PLAN_MISMATCH, skipping that work, if not).
+ *   kv_indices device int32 [kv_indptr[B]]: KV row of every token.
+ *   out        device bf16 [B,16,512], 16-byte aligned; fully written (an empty
+ *              sequence yields zeros).
+ *   sm_scale   softmax scale (the pages use 1/sqrt(576)).
+ *   dtype_mode an mla_dtype_mode.
+ *   workspace  the plan from mla_decode_plan for this batch / kv_indptr.
+ *   stream     cudaStream_t.
+ * Never allocates, never synchronises. A plan's workspace serves one decode at
+ * a time: decodes sharing a plan must be ordered (same stream or events).
+ * Errors detected on the host return immediately (MLA_ERR_ARG, MLA_ERR_DTYPE,
+ * MLA_ERR_ALIGN, MLA_ERR_DEVICE, MLA_ERR_CUDA for a failed launch); errors found
+ * by the kernel are recorded in the plan's error word (mla_plan_check_error).
+ */
+int mla_decode(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+               const int32_t* kv_indices, void* out, float sm_scale, int dtype_mode, mla_plan* workspace,
+               void* stream);
+
+/*
+ * mla_decode_stage1 — only the persistent stage-1 kernel of mla_decode (the
+ * pages' direct mla_decode_stage1_asm_fwd call, submission 690201 "V6c",
+ * custom_kernel). Sequences the plan keeps whole get their final bf16 output
+ * in out; split sequences get fp32 partial (O, LSE) in the workspace, which
+ * mla_decode_reduce then merges. Arguments as for mla_decode.
+ */
+int mla_decode_stage1(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+                      const int32_t* kv_indices, void* out, float sm_scale, int dtype_mode, mla_plan* workspace,
+                      void* stream);
+
+/*
+ * mla_decode_reduce — LSE-combine of the split sequences' partial results into
+ * bf16 out (the pages' mla_reduce_v1 call, submission 690201 "V6c",
+ * custom_kernel): per head, L = log sum_s e^{lse_s} and
+ * out = sum_s e^{lse_s - L} * O_s. No-op when the plan splits no sequence.
+ */
+int mla_decode_reduce(void* out, mla_plan* workspace, void* stream);
+
+/*
+ * mla_plan_check_error — synchronise stream, read and clear the error word the
+ * kernels set (MLA_OK, MLA_ERR_TIMEOUT, MLA_ERR_PLAN_MISMATCH, MLA_ERR_INDEX).
+ */
+int mla_plan_check_error(mla_plan* plan, void* stream);
+
+/*
+ * mla_plan_compute_host — the planner alone, on the host, with no CUDA call
+ * (for inspection and testing; mla_decode_plan runs the same code).
+ *   counts      host int32 [4] (required): number of work items, CTAs that get
+ *               work, partial slots, split sequences.
+ *   items       host int32 [items_cap][5] or NULL: per work item (sequence b,
+ *               first row, end row, partial slot or -1 for a final write,
+ *               sequence length), grouped by CTA in CTA order.
+ *   work_indptr host int32 [indptr_cap] or NULL: CTA c owns items
+ *               [work_indptr[c], work_indptr[c+1]); needs num_ctas + 1 entries.
+ *   reduce      host int32 [reduce_cap][3] or NULL: per split sequence (b,
+ *               first slot, slot count).
+ * An array whose capacity is too small is left untouched (call once with NULL
+ * arrays to size them). Errors: MLA_ERR_ARG, MLA_ERR_INDPTR, MLA_ERR_NOMEM.
+ */
+int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
+                          int32_t* counts, int32_t* items, int items_cap, int32_t* work_indptr, int indptr_cap,
+                          int32_t* reduce, int reduce_cap);
+
+/* Human-readable name of a status code (static string). */
+const char* mla_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

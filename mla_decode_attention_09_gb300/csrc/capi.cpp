@@ -1,0 +1,318 @@
+// C ABI of the MLA decode library: plan lifetime and caching, argument
+// validation, and the stage-1 / reduce launches. No exception leaves this file.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+struct mla_plan {
+  int device = -1;
+  int refcount = 0;
+  int batch = 0;
+  int num_sms = 0;
+  mla::PlanOptions opt;
+  std::vector<int32_t> indptr;   // cache key contents
+  mla::HostPlan host;
+  mla::DevicePlan dev{};
+  void* block = nullptr;         // single device allocation backing every buffer
+  size_t block_bytes = 0;
+  const void* zero_row = nullptr;  // 1152 zero bytes (source for tail rows of a tile)
+};
+
+namespace {
+
+std::mutex g_mu;
+std::vector<mla_plan*> g_cache;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, int num_sms,
+              const mla::PlanOptions& o) {
+  return p->device == device && p->batch == batch && p->num_sms == num_sms &&
+         p->opt.num_kv_slots == o.num_kv_slots && p->opt.min_rows_per_split == o.min_rows_per_split &&
+         p->opt.granularity == o.granularity && p->opt.ctas_per_sm == o.ctas_per_sm &&
+         std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0;
+}
+
+void destroy_plan(mla_plan* p) {
+  if (p->block) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaFree(p->block);
+    if (cur != p->device && cur >= 0) cudaSetDevice(cur);
+  }
+  mla::free_host_plan(&p->host);
+  delete p;
+}
+
+int check_device(int* device_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MLA_ERR_DEVICE;
+  if (major != 10 || minor != 3) return MLA_ERR_DEVICE;  // kernels are built for sm_103a only
+  *device_out = dev;
+  return MLA_OK;
+}
+
+int make_plan(int batch, const int32_t* kv_indptr_host, int num_sms, const mla::PlanOptions& opt, int device,
+              mla_plan** out) {
+  mla_plan* p = new (std::nothrow) mla_plan();
+  if (!p) return MLA_ERR_NOMEM;
+  p->device = device;
+  p->batch = batch;
+  p->num_sms = num_sms;
+  p->opt = opt;
+  p->indptr.assign(kv_indptr_host, kv_indptr_host + batch + 1);
+  int rc = mla::build_host_plan(batch, kv_indptr_host, num_sms, opt, &p->host);
+  if (rc != MLA_OK) {
+    delete p;
+    return rc;
+  }
+  const mla::HostPlan& h = p->host;
+  // layout of the single device block
+  size_t off = 0;
+  const size_t o_items = off;
+  off = align_up(off + sizeof(mla::WorkItem) * (size_t)h.n_items, 256);
+  const size_t o_indptr = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)(h.num_ctas + 1), 256);
+  const size_t o_reduce = off;
+  off = align_up(off + sizeof(mla::ReduceEntry) * (size_t)h.n_reduce, 256);
+  const size_t o_po = off;
+  off = align_up(off + sizeof(float) * (size_t)h.num_slots * mla::kHeads * mla::kVDim, 256);
+  const size_t o_lse = off;
+  off = align_up(off + sizeof(float) * (size_t)h.num_slots * mla::kHeads, 256);
+  const size_t o_err = off;
+  off = align_up(off + sizeof(int), 256);
+  const size_t o_zero = off;
+  off = align_up(off + mla::kQkDim * 2, 256);
+  p->block_bytes = off;
+  if (cudaMalloc(&p->block, off) != cudaSuccess) {
+    cudaGetLastError();
+    p->block = nullptr;
+    destroy_plan(p);
+    return MLA_ERR_NOMEM;
+  }
+  char* base = static_cast<char*>(p->block);
+  std::vector<char> staging(o_po, 0);  // items, indptr and reduce map, uploaded in one copy
+  if (h.n_items) std::memcpy(staging.data() + o_items, h.items, sizeof(mla::WorkItem) * (size_t)h.n_items);
+  std::memcpy(staging.data() + o_indptr, h.work_indptr, sizeof(int32_t) * (size_t)(h.num_ctas + 1));
+  if (h.n_reduce) std::memcpy(staging.data() + o_reduce, h.reduce, sizeof(mla::ReduceEntry) * (size_t)h.n_reduce);
+  if (cudaMemcpy(base, staging.data(), o_po, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(base + o_err, 0, off - o_err) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    destroy_plan(p);
+    return MLA_ERR_CUDA;
+  }
+  p->dev.items = reinterpret_cast<const mla::WorkItem*>(base + o_items);
+  p->dev.work_indptr = reinterpret_cast<const int32_t*>(base + o_indptr);
+  p->dev.reduce = reinterpret_cast<const mla::ReduceEntry*>(base + o_reduce);
+  p->dev.part_o = reinterpret_cast<float*>(base + o_po);
+  p->dev.part_lse = reinterpret_cast<float*>(base + o_lse);
+  p->dev.err = reinterpret_cast<int*>(base + o_err);
+  p->dev.num_kv_slots = opt.num_kv_slots;
+  p->dev.num_ctas = h.num_ctas;
+  p->dev.n_reduce = h.n_reduce;
+  p->zero_row = base + o_zero;
+  p->refcount = 1;
+  *out = p;
+  return MLA_OK;
+}
+
+int validate_decode(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+                    const int32_t* kv_indices, const void* out, int dtype_mode, const mla_plan* plan) {
+  if (!plan || plan->refcount <= 0) return MLA_ERR_ARG;
+  if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8) return MLA_ERR_DTYPE;
+  if (plan->batch > 0) {
+    if (!q || !kv || !kv_indptr || !out) return MLA_ERR_ARG;
+    if (plan->host.total_rows > 0 && !kv_indices) return MLA_ERR_ARG;
+    if (dtype_mode == MLA_MODE_FP8 && !kv_scale) return MLA_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(out)) & 15)
+      return MLA_ERR_ALIGN;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return MLA_ERR_DEVICE;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
+                       mla_plan** plan_out) {
+  try {
+    if (!plan_out || batch < 0 || (!kv_indptr_host && batch > 0)) return MLA_ERR_ARG;
+    *plan_out = nullptr;
+    int device = -1;
+    int rc = check_device(&device);
+    if (rc != MLA_OK) return rc;
+    if (num_sms <= 0) {
+      if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    }
+    const mla::PlanOptions opt = mla::resolve_options(options);
+    static const int32_t kZero = 0;
+    const int32_t* indptr = batch > 0 ? kv_indptr_host : &kZero;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (mla_plan* p : g_cache) {
+      if (same_key(p, device, batch, indptr, num_sms, opt)) {
+        ++p->refcount;
+        *plan_out = p;
+        return MLA_OK;
+      }
+    }
+    mla_plan* p = nullptr;
+    rc = make_plan(batch, indptr, num_sms, opt, device, &p);
+    if (rc != MLA_OK) return rc;
+    g_cache.push_back(p);
+    *plan_out = p;
+    return MLA_OK;
+  } catch (...) {
+    return MLA_ERR_NOMEM;
+  }
+}
+
+int mla_decode_plan(int batch, const int32_t* kv_indptr_host, int num_sms, mla_plan** plan_out) {
+  return mla_decode_plan_ex(batch, kv_indptr_host, num_sms, nullptr, plan_out);
+}
+
+int mla_plan_release(mla_plan* plan) {
+  if (!plan) return MLA_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (size_t i = 0; i < g_cache.size(); ++i) {
+    if (g_cache[i] == plan) {
+      if (--plan->refcount == 0) {
+        g_cache.erase(g_cache.begin() + (long)i);
+        destroy_plan(plan);
+      }
+      return MLA_OK;
+    }
+  }
+  return MLA_ERR_ARG;
+}
+
+int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
+  if (!plan || !info) return MLA_ERR_ARG;
+  info->batch = plan->batch;
+  info->num_ctas = plan->host.num_ctas;
+  info->num_work_items = plan->host.n_items;
+  info->num_partial_slots = plan->host.num_slots;
+  info->num_split_seqs = plan->host.n_reduce;
+  info->device = plan->device;
+  info->total_rows = plan->host.total_rows;
+  info->max_rows_per_cta = plan->host.max_rows_per_cta;
+  info->workspace_bytes = plan->block_bytes;
+  return MLA_OK;
+}
+
+int mla_decode_stage1(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+                      const int32_t* kv_indices, void* out, float sm_scale, int dtype_mode, mla_plan* workspace,
+                      void* stream) {
+  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace);
+  if (rc != MLA_OK) return rc;
+  if (workspace->batch == 0) return MLA_OK;
+  const mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
+  return mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream) == 0 ? MLA_OK
+                                                                                             : MLA_ERR_CUDA;
+}
+
+int mla_decode_reduce(void* out, mla_plan* workspace, void* stream) {
+  if (!workspace || workspace->refcount <= 0) return MLA_ERR_ARG;
+  if (workspace->dev.n_reduce == 0) return MLA_OK;
+  if (!out) return MLA_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 15) return MLA_ERR_ALIGN;
+  return mla::launch_reduce(out, workspace->dev, stream, false) == 0 ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+               const int32_t* kv_indices, void* out, float sm_scale, int dtype_mode, mla_plan* workspace,
+               void* stream) {
+  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace);
+  if (rc != MLA_OK) return rc;
+  if (workspace->batch == 0) return MLA_OK;
+  const mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
+  if (mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream) != 0) return MLA_ERR_CUDA;
+  // the reduce is launched programmatically dependent: it starts while stage 1
+  // drains and waits for its results on the device
+  if (mla::launch_reduce(out, workspace->dev, stream, true) != 0) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_plan_check_error(mla_plan* plan, void* stream) {
+  if (!plan || plan->refcount <= 0) return MLA_ERR_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, plan->dev.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (code != 0 && cudaMemset(plan->dev.err, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+  return code;
+}
+
+const char* mla_strerror(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_ARG: return "invalid argument";
+    case MLA_ERR_DTYPE: return "unknown dtype_mode";
+    case MLA_ERR_PLAN_MISMATCH: return "device kv_indptr does not match the plan";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_TIMEOUT: return "a bounded wait in a kernel timed out";
+    case MLA_ERR_ALIGN: return "q, kv or out is not 16-byte aligned";
+    case MLA_ERR_NOMEM: return "allocation failed";
+    case MLA_ERR_INDEX: return "kv_indices entry out of range";
+    case MLA_ERR_DEVICE: return "no usable sm_103 device or wrong device for the plan";
+    case MLA_ERR_INDPTR: return "kv_indptr must start at 0 and be non-decreasing";
+    default: return "unknown status";
+  }
+}
+
+int mla_version(void) { return 100; }
+
+// Host-only view of the planner (no CUDA call): fills caller arrays with the
+// work list the plan would hold. Any output pointer may be NULL to only count.
+int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
+                          int32_t* counts4, int32_t* items5, int items_cap, int32_t* work_indptr, int indptr_cap,
+                          int32_t* reduce3, int reduce_cap) {
+  try {
+    if (!counts4) return MLA_ERR_ARG;
+    mla::HostPlan h;
+    static const int32_t kZero = 0;
+    int rc = mla::build_host_plan(batch, batch > 0 ? kv_indptr_host : &kZero, num_sms, mla::resolve_options(options),
+                                  &h);
+    if (rc != MLA_OK) return rc;
+    counts4[0] = h.n_items;
+    counts4[1] = h.num_ctas;
+    counts4[2] = h.num_slots;
+    counts4[3] = h.n_reduce;
+    if (items5 && items_cap >= h.n_items)
+      for (int i = 0; i < h.n_items; ++i) {
+        items5[5 * i + 0] = h.items[i].b;
+        items5[5 * i + 1] = h.items[i].t_begin;
+        items5[5 * i + 2] = h.items[i].t_end;
+        items5[5 * i + 3] = h.items[i].slot;
+        items5[5 * i + 4] = h.items[i].seq_len;
+      }
+    if (work_indptr && indptr_cap >= h.num_ctas + 1)
+      std::memcpy(work_indptr, h.work_indptr, sizeof(int32_t) * (size_t)(h.num_ctas + 1));
+    if (reduce3 && reduce_cap >= h.n_reduce)
+      for (int i = 0; i < h.n_reduce; ++i) {
+        reduce3[3 * i + 0] = h.reduce[i].b;
+        reduce3[3 * i + 1] = h.reduce[i].slot_begin;
+        reduce3[3 * i + 2] = h.reduce[i].n_slots;
+      }
+    mla::free_host_plan(&h);
+    return MLA_OK;
+  } catch (...) {
+    return MLA_ERR_NOMEM;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,156 @@
+// Host split-KV planner.
+//
+// The pages build a persistent-mode work list on the host side of every call
+// shape and cache it (get_mla_metadata_info_v1 / get_mla_metadata_v1 in
+// kernelbot amd-mixed-mla submission 598454 "v12", _get_or_compute_metadata;
+// kv_granularity = max(page_size, 16) there). Their field layout belongs to a
+// closed library and is not shown, so this planner defines its own: the rows
+// of all sequences, laid end to end, are cut into one contiguous range per
+// persistent CTA of nearly equal length. A sequence that lies inside one range
+// is a single work item writing its final output; a sequence that straddles
+// cuts becomes several items writing partial (O, LSE) slots that the reduce
+// merges. Cuts fall on multiples of `granularity` rows from the sequence
+// start, and no range is shorter than `min_rows_per_split` unless the whole
+// problem is.
+#include <algorithm>
+#include <utility>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+namespace mla {
+
+PlanOptions resolve_options(const mla_plan_options* o) {
+  PlanOptions r;
+  if (!o) return r;
+  if (o->num_kv_slots > 0) r.num_kv_slots = o->num_kv_slots;
+  if (o->min_rows_per_split > 0) r.min_rows_per_split = o->min_rows_per_split;
+  if (o->granularity > 0) r.granularity = o->granularity;
+  if (o->ctas_per_sm > 0) r.ctas_per_sm = o->ctas_per_sm;
+  return r;
+}
+
+void free_host_plan(HostPlan* p) {
+  std::free(p->items);
+  std::free(p->work_indptr);
+  std::free(p->reduce);
+  p->items = nullptr;
+  p->work_indptr = nullptr;
+  p->reduce = nullptr;
+}
+
+int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const PlanOptions& opt, HostPlan* out) {
+  if (batch < 0 || num_sms <= 0 || !out || (batch > 0 && !kv_indptr)) return MLA_ERR_ARG;
+  if (opt.granularity <= 0 || opt.min_rows_per_split <= 0 || opt.ctas_per_sm <= 0) return MLA_ERR_ARG;
+  *out = HostPlan{};
+  out->batch = batch;
+  if (batch > 0 && kv_indptr[0] != 0) return MLA_ERR_INDPTR;
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (kv_indptr[b + 1] < kv_indptr[b]) return MLA_ERR_INDPTR;
+    total += (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+  }
+  out->total_rows = total;
+
+  const int64_t G = opt.granularity;
+  const int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
+  int64_t target = total > 0 ? (total + max_ctas - 1) / max_ctas : 1;
+  target = std::max<int64_t>(target, opt.min_rows_per_split);
+  target = (target + G - 1) / G * G;
+  const int64_t n_ranges = total > 0 ? std::min<int64_t>(max_ctas, (total + target - 1) / target) : 1;
+
+  // Global cut points: the ideal cut k * total / n, moved to the nearest
+  // multiple of G from the start of the sequence it falls in (or to that
+  // sequence's start / end when less than G rows would be left on a side).
+  // Cuts are absolute, so snapping errors never accumulate.
+  std::vector<int64_t> cuts((size_t)n_ranges + 1, 0);
+  cuts[(size_t)n_ranges] = total;
+  for (int64_t k = 1; k < n_ranges; ++k) {
+    const int64_t P = total * k / n_ranges;
+    // sequence containing row P: last b with kv_indptr[b] <= P (it is non-empty since P < total)
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if ((int64_t)kv_indptr[mid] <= P) lo = mid; else hi = mid - 1;
+    }
+    const int64_t S = kv_indptr[lo], L = (int64_t)kv_indptr[lo + 1] - S;
+    int64_t r = (P - S + G / 2) / G * G;
+    if (r < G) r = 0;
+    if (L - r < G) r = L;
+    cuts[(size_t)k] = std::max(cuts[(size_t)k - 1], S + r);
+  }
+  std::vector<std::pair<int64_t, int64_t>> ranges;  // non-empty CTA row ranges, in order
+  for (int64_t k = 0; k < n_ranges; ++k)
+    if (cuts[(size_t)k + 1] > cuts[(size_t)k]) ranges.emplace_back(cuts[(size_t)k], cuts[(size_t)k + 1]);
+  if (ranges.empty()) ranges.emplace_back(0, 0);  // no rows at all: one CTA writes the zero outputs
+
+  std::vector<WorkItem> items;
+  std::vector<int32_t> cta_of_item;
+  items.reserve((size_t)batch + ranges.size() * 2);
+  size_t cta = 0;
+  const size_t last = ranges.size() - 1;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t S = kv_indptr[b], E = kv_indptr[b + 1];
+    while (cta < last && ranges[cta].second <= S) ++cta;
+    if (S == E) {  // empty sequence: a zero-row item that writes zeros
+      items.push_back(WorkItem{b, 0, 0, -1, 0, {0, 0, 0}});
+      cta_of_item.push_back((int32_t)cta);
+      continue;
+    }
+    while (true) {
+      const int64_t a = std::max(S, ranges[cta].first), e = std::min(E, ranges[cta].second);
+      if (e > a) {
+        items.push_back(WorkItem{b, (int32_t)(a - S), (int32_t)(e - S), -1, (int32_t)(E - S), {0, 0, 0}});
+        cta_of_item.push_back((int32_t)cta);
+      }
+      if (E <= ranges[cta].second || cta == last) break;
+      ++cta;
+    }
+  }
+  const int64_t used_ctas = (int64_t)ranges.size();
+
+  // Partial slots for sequences cut into several items (their items are adjacent).
+  std::vector<ReduceEntry> reduce;
+  int slot = 0;
+  for (size_t i = 0; i < items.size();) {
+    size_t j = i + 1;
+    while (j < items.size() && items[j].b == items[i].b) ++j;
+    if (j - i > 1) {
+      reduce.push_back(ReduceEntry{items[i].b, slot, (int32_t)(j - i), 0});
+      for (size_t k = i; k < j; ++k) items[k].slot = slot++;
+    }
+    i = j;
+  }
+
+  // Items are already grouped by CTA in increasing order: CSR offsets.
+  std::vector<int32_t> indptr((size_t)used_ctas + 1, 0);
+  for (size_t i = 0; i < items.size(); ++i) indptr[(size_t)cta_of_item[i] + 1]++;
+  for (int64_t c = 0; c < used_ctas; ++c) indptr[(size_t)c + 1] += indptr[(size_t)c];
+  int64_t max_rows = 0;
+  for (int64_t c = 0; c < used_ctas; ++c) {
+    int64_t r = 0;
+    for (int32_t i = indptr[(size_t)c]; i < indptr[(size_t)c + 1]; ++i) r += items[(size_t)i].t_end - items[(size_t)i].t_begin;
+    max_rows = std::max(max_rows, r);
+  }
+
+  out->num_ctas = (int)used_ctas;
+  out->num_slots = slot;
+  out->n_items = (int)items.size();
+  out->n_reduce = (int)reduce.size();
+  out->max_rows_per_cta = max_rows;
+  out->items = (WorkItem*)std::malloc(sizeof(WorkItem) * std::max<size_t>(items.size(), 1));
+  out->work_indptr = (int32_t*)std::malloc(sizeof(int32_t) * indptr.size());
+  out->reduce = (ReduceEntry*)std::malloc(sizeof(ReduceEntry) * std::max<size_t>(reduce.size(), 1));
+  if (!out->items || !out->work_indptr || !out->reduce) {
+    free_host_plan(out);
+    return MLA_ERR_NOMEM;
+  }
+  if (!items.empty()) std::memcpy(out->items, items.data(), sizeof(WorkItem) * items.size());
+  std::memcpy(out->work_indptr, indptr.data(), sizeof(int32_t) * indptr.size());
+  if (!reduce.empty()) std::memcpy(out->reduce, reduce.data(), sizeof(ReduceEntry) * reduce.size());
+  return MLA_OK;
+}
+
+}  // namespace mla

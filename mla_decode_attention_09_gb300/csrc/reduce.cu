@@ -1,0 +1,72 @@
+// Split reduce of MLA decode: merges the normalised fp32 partial outputs of a
+// sequence that stage 1 processed in several KV chunks (the pages'
+// mla_reduce_v1 call after mla_decode_stage1_asm_fwd, kernelbot amd-mixed-mla
+// submission 690201 "V6c", custom_kernel). For each head, with base-2
+// log-sum-exps lse_s of the chunks, L = log2 sum_s 2^{lse_s} and
+// out = sum_s 2^{lse_s - L} O_s, rounded to bf16.
+//
+// One CTA of 128 threads per (split sequence, head); each thread owns 4 of the
+// 512 output dims, so every partial row is read once with 16-byte loads.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kReduceThreads = kVDim / 4;  // 128
+
+__global__ void __launch_bounds__(kReduceThreads)
+    mla_reduce_kernel(const DevicePlan p, __nv_bfloat16* __restrict__ out, int use_pdl) {
+  if (use_pdl) ptx::griddep_wait();  // stage 1 of this decode has finished writing the partials
+  const int e = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
+  if (e >= p.n_reduce) return;
+  const ReduceEntry r = p.reduce[e];
+  const float* lse = p.part_lse + (int64_t)r.slot_begin * kHeads + h;
+  float m = -INFINITY;
+  for (int s = 0; s < r.n_slots; ++s) m = fmaxf(m, lse[(int64_t)s * kHeads]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (m != -INFINITY) {
+    float z = 0.f;
+    for (int s = 0; s < r.n_slots; ++s) z += exp2f(lse[(int64_t)s * kHeads] - m);
+    const float inv_z = 1.0f / z;
+    const float* po = p.part_o + ((int64_t)r.slot_begin * kHeads + h) * kVDim + 4 * threadIdx.x;
+    for (int s = 0; s < r.n_slots; ++s) {
+      const float wgt = exp2f(lse[(int64_t)s * kHeads] - m) * inv_z;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(po + (int64_t)s * kHeads * kVDim));
+      acc.x += wgt * v.x;
+      acc.y += wgt * v.y;
+      acc.z += wgt * v.z;
+      acc.w += wgt * v.w;
+    }
+  }
+  uint2 packed;
+  packed.x = ptx::pack_bf16x2(acc.x, acc.y);
+  packed.y = ptx::pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(out + ((int64_t)r.b * kHeads + h) * kVDim + 4 * threadIdx.x) = packed;
+}
+
+}  // namespace
+
+int launch_reduce(void* out, const DevicePlan& p, void* stream, bool pdl) {
+  if (p.n_reduce <= 0) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.n_reduce * kHeads));
+  cfg.blockDim = dim3(kReduceThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t err =
+      cudaLaunchKernelEx(&cfg, mla_reduce_kernel, p, static_cast<__nv_bfloat16*>(out), pdl ? 1 : 0);
+  return (int)err;
+}
+
+}  // namespace mla

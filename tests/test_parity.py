@@ -1,0 +1,176 @@
+"""GPU parity: the CUDA library (through the C ABI) against the float64 oracle,
+element by element, on the same seeded inputs.
+
+Tolerances (max-abs error, relative L2 error of the whole output):
+bf16 2e-2 / 1e-2, fp8 6e-2 / 3e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {mi.MODE_BF16: (2e-2, 1e-2), mi.MODE_FP8: (6e-2, 3e-2)}
+
+
+@pytest.fixture(scope="module")
+def mla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_decode_attention_09_gb300 import build
+    build.build()
+    import mla_decode_attention_09_gb300 as m
+    return m
+
+
+def run(mla, inp: mi.Inputs, num_sms=0, **opts):
+    d = inp.to("cuda")
+    plan = mla.plan(inp.kv_indptr, num_sms, num_kv_slots=max(inp.kv.shape[0], 1), **opts)
+    out = torch.full((inp.batch, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.decode(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, out, sm_scale=inp.sm_scale,
+               dtype_mode=inp.mode, plan=plan)
+    assert plan.check_error() == 0
+    return out, plan
+
+
+def compare(got: torch.Tensor, ref: np.ndarray, mode: int, what: str = ""):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    denom = float(np.linalg.norm(ref))
+    rel_l2 = float(np.linalg.norm(g - ref) / denom) if denom > 0 else float(np.linalg.norm(g - ref))
+    atol, rtol = TOL[mode]
+    assert max_abs <= atol and rel_l2 <= rtol, f"{what}: max_abs={max_abs:.3e} rel_l2={rel_l2:.3e}"
+    return max_abs, rel_l2
+
+
+def oracle_out(inp: mi.Inputs, seq_ids=None):
+    out, _ = oracle.decode(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, inp.sm_scale, inp.mode, inp.kv_scale,
+                           seq_ids=seq_ids)
+    return out
+
+
+ODD = [1, 15, 17, 63, 64, 65, 1000, 0, 129, 2]
+
+
+@pytest.mark.parametrize("mode", [mi.MODE_BF16, mi.MODE_FP8])
+@pytest.mark.parametrize("split", ["whole", "split"])
+def test_odd_lengths(mla, mode, split):
+    inp = mi.make_inputs(ODD, mode, seed=100 + mode, permute=True, extra_slots=37)
+    opts = {} if split == "whole" else {"min_rows_per_split": 16}
+    out, plan = run(mla, inp, num_sms=152 if split == "whole" else 5, **opts)
+    info = plan.info()
+    if split == "split":
+        assert info["num_split_seqs"] > 0
+    compare(out, oracle_out(inp), mode, f"odd lengths {split}")
+
+
+@pytest.mark.parametrize("mode", [mi.MODE_BF16, mi.MODE_FP8])
+def test_one_long_sequence_many_splits(mla, mode):
+    inp = mi.make_inputs([5003], mode, seed=7)
+    out, plan = run(mla, inp, num_sms=152, min_rows_per_split=16)
+    assert plan.info()["num_partial_slots"] > 100
+    compare(out, oracle_out(inp), mode, "one long sequence")
+
+
+@pytest.mark.parametrize("mode", [mi.MODE_BF16, mi.MODE_FP8])
+def test_peaked_scores(mla, mode):
+    # larger query norm -> sharply peaked softmax; exercises the running-max rescale
+    inp = mi.make_inputs([300, 1, 77], mode, seed=9, q_std=6.0)
+    out, _ = run(mla, inp, num_sms=4, min_rows_per_split=16)
+    compare(out, oracle_out(inp), mode, "peaked")
+
+
+def test_fp8_query_cast_saturates(mla):
+    # entries beyond +-448 exercise the saturating direct cast of the query
+    inp = mi.make_inputs([40, 9], mi.MODE_FP8, seed=13)
+    inp.q[0, 3, :50] = 1000.0
+    inp.q[1, 5, 100:140] = -600.0
+    out, _ = run(mla, inp)
+    ref = oracle_out(inp)
+    compare(out, ref, mi.MODE_FP8, "fp8 saturation")
+
+
+@pytest.mark.parametrize("mode", [mi.MODE_BF16, mi.MODE_FP8])
+def test_stage1_plus_reduce_equals_decode_and_is_deterministic(mla, mode):
+    inp = mi.make_inputs([700, 333, 64], mode, seed=21)
+    a, plan = run(mla, inp, num_sms=6, min_rows_per_split=16)
+    b, _ = run(mla, inp, num_sms=6, min_rows_per_split=16)
+    assert torch.equal(a, b)
+    d = inp.to("cuda")
+    c = torch.empty_like(a)
+    mla.decode_stage1(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, c, plan=plan,
+                      sm_scale=inp.sm_scale, dtype_mode=mode)
+    mla.decode_reduce(c, plan=plan)
+    assert plan.check_error() == 0
+    assert torch.equal(a, c)
+
+
+def test_empty_batch_and_empty_sequences(mla):
+    inp = mi.make_inputs([0, 0, 0], mi.MODE_BF16, seed=1, extra_slots=4)
+    out, _ = run(mla, inp)
+    assert torch.count_nonzero(out) == 0
+    inp0 = mi.make_inputs([], mi.MODE_FP8, seed=1, extra_slots=4)
+    out0, _ = run(mla, inp0)
+    assert out0.shape == (0, 16, 512)
+
+
+def test_plan_mismatch_is_reported(mla):
+    inp = mi.make_inputs([100, 50], mi.MODE_BF16, seed=3)
+    d = inp.to("cuda")
+    plan = mla.plan(torch.tensor([0, 60, 150], dtype=torch.int32), 0, num_kv_slots=inp.kv.shape[0])
+    out = torch.zeros((2, 16, 512), dtype=torch.bfloat16, device="cuda")
+    mla.decode(d.q, d.kv, None, d.kv_indptr, d.kv_indices, out, dtype_mode=0, plan=plan)
+    assert plan.check_error() == -3   # MLA_ERR_PLAN_MISMATCH
+    assert plan.check_error() == 0    # cleared after reading
+
+
+def test_out_of_range_index_is_reported(mla):
+    inp = mi.make_inputs([30, 20], mi.MODE_FP8, seed=4)
+    inp.kv_indices[7] = inp.kv.shape[0] + 5
+    out, plan = None, None
+    d = inp.to("cuda")
+    plan = mla.plan(inp.kv_indptr, 0, num_kv_slots=inp.kv.shape[0])
+    out = torch.zeros((2, 16, 512), dtype=torch.bfloat16, device="cuda")
+    mla.decode(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, out, plan=plan)
+    assert plan.check_error() == -8   # MLA_ERR_INDEX; the bad row was read as zeros
+    assert torch.isfinite(out.float()).all()
+
+
+def test_host_argument_errors(mla):
+    inp = mi.make_inputs([10], mi.MODE_BF16, seed=2).to("cuda")
+    plan = mla.plan(inp.kv_indptr.cpu(), 0)
+    out = torch.empty((1, 16, 512), dtype=torch.bfloat16, device="cuda")
+    lib = mla.load_library()
+    s = torch.cuda.current_stream().cuda_stream
+    args = [inp.q.data_ptr(), inp.kv.data_ptr(), None, inp.kv_indptr.data_ptr(), inp.kv_indices.data_ptr(),
+            out.data_ptr(), 0.04, 0, plan.handle, s]
+    bad = list(args); bad[7] = 5
+    assert lib.mla_decode(*bad) == -2            # dtype
+    bad = list(args); bad[0] = inp.q.data_ptr() + 2
+    assert lib.mla_decode(*bad) == -6            # alignment
+    bad = list(args); bad[7] = 1
+    assert lib.mla_decode(*bad) == -1            # fp8 without kv_scale
+    assert lib.mla_decode(*args) == 0
+    assert plan.check_error() == 0
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+SAMPLES = {"bf16_b4_l1024": None, "fp8_b4_l8192": None, "fp8_b64_l1024": [0, 17, 38, 63],
+           "fp8_b64_l8192": [0, 21, 42, 63], "bf16_b128_ragged": [0, 31, 77, 127]}
+
+
+@pytest.mark.parametrize("name", list(mi.WORKLOADS))
+def test_full_size_workload(mla, name):
+    inp = mi.make_workload(name)
+    out, plan = run(mla, inp)   # default plan: the launch configuration the benchmark times
+    ids = SAMPLES[name]
+    ref = oracle_out(inp, seq_ids=ids)
+    got = out if ids is None else out[torch.tensor(ids, device="cuda")]
+    compare(got, ref, inp.mode, name)
+    assert torch.isfinite(out.float()).all()

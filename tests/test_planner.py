@@ -1,0 +1,101 @@
+"""CPU tests of the host split-KV planner (through the C ABI's host-only entry)."""
+import numpy as np
+import pytest
+
+import mla_decode_attention_09_gb300 as mla
+
+
+def _check_plan(lengths, num_sms, **opts):
+    ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+    ip[1:] = np.cumsum(lengths)
+    r = mla.plan_compute_host(ip, num_sms, **opts)
+    items, wip, red = r["items"], r["work_indptr"], r["reduce"]
+    G = opts.get("granularity", 16)
+    min_split = opts.get("min_rows_per_split", 256)
+    cpsm = opts.get("ctas_per_sm", 1)
+    total = int(ip[-1])
+    # CTA ranges: CSR over the item list, at most num_sms * ctas_per_sm CTAs
+    assert wip[0] == 0 and wip[-1] == len(items) and np.all(np.diff(wip) >= 0)
+    assert 1 <= r["num_ctas"] <= num_sms * cpsm or (len(lengths) == 0 and r["num_ctas"] <= 1)
+    # every row of every sequence covered exactly once, in order
+    by_seq = {}
+    for b, t0, t1, slot, L in items:
+        assert 0 <= b < len(lengths) and L == lengths[b]
+        by_seq.setdefault(int(b), []).append((int(t0), int(t1), int(slot)))
+    assert sorted(by_seq) == list(range(len(lengths)))
+    next_slot = 0
+    red_map = {int(b): (int(s0), int(n)) for b, s0, n in red}
+    for b, parts in by_seq.items():
+        L = lengths[b]
+        pos = 0
+        for t0, t1, _ in parts:
+            assert t0 == pos and t1 >= t0
+            if t1 != L:
+                assert t1 % G == 0, "cuts fall on the granularity"
+            pos = t1
+        assert pos == L
+        if len(parts) == 1:
+            assert parts[0][2] == -1 and b not in red_map
+        else:
+            s0, n = red_map[b]
+            assert n == len(parts) and [p[2] for p in parts] == list(range(s0, s0 + n))
+            assert s0 == next_slot
+            next_slot += n
+            assert all(t1 > t0 for t0, t1, _ in parts), "no empty partial"
+    assert next_slot == r["num_slots"]
+    # load balance: no CTA above the target (rounded to G) plus two granules
+    if total:
+        max_ctas = num_sms * cpsm
+        target = max(-(-total // max_ctas), min_split)
+        target = -(-target // G) * G
+        rows = [sum(int(items[i, 2] - items[i, 1]) for i in range(wip[c], wip[c + 1])) for c in range(r["num_ctas"])]
+        # each cut moves less than G from its ideal position
+        assert max(rows) <= target + 2 * G
+        assert sum(rows) == total
+    return r
+
+
+@pytest.mark.parametrize("lengths,num_sms", [
+    ([1024] * 4, 152), ([8192] * 4, 152), ([1024] * 64, 152), ([8192] * 64, 152),
+    ([1], 152), ([0], 152), ([0, 5, 0], 4), ([17, 15, 1000, 63, 64, 65], 3), ([1000], 1),
+    ([4096] * 3, 2), (list(range(0, 300, 7)), 5),
+])
+def test_plan_invariants(lengths, num_sms):
+    _check_plan(lengths, num_sms)
+
+
+def test_plan_invariants_random():
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        B = int(rng.integers(1, 40))
+        lengths = [int(x) for x in rng.integers(0, 3000, B)]
+        if rng.random() < 0.2:
+            lengths[int(rng.integers(0, B))] = 0
+        opts = {}
+        if rng.random() < 0.5:
+            opts["min_rows_per_split"] = int(rng.choice([16, 64, 256, 1024]))
+        if rng.random() < 0.3:
+            opts["granularity"] = int(rng.choice([1, 8, 16, 64]))
+        _check_plan(lengths, int(rng.integers(1, 160)), **opts)
+
+
+def test_plan_headline_shapes():
+    # B=64 x 8192 over 152 SMs: every SM busy, each sequence split in 2-4 chunks
+    r = _check_plan([8192] * 64, 152)
+    assert r["num_ctas"] == 152
+    assert 64 * 2 <= r["num_slots"] <= 64 * 4
+    # B=4 x 1024 bf16: small problem, minimum chunk keeps the split count low
+    r = _check_plan([1024] * 4, 152)
+    assert r["num_ctas"] == 16
+
+
+def test_plan_rejects_bad_indptr():
+    with pytest.raises(mla.MLAError) as e:
+        mla.plan_compute_host(np.array([0, 5, 3], dtype=np.int32), 4)
+    assert e.value.status == -10
+    with pytest.raises(mla.MLAError) as e:
+        mla.plan_compute_host(np.array([1, 5], dtype=np.int32), 4)
+    assert e.value.status == -10
+    with pytest.raises(mla.MLAError) as e:
+        mla.plan_compute_host(np.array([0, 5], dtype=np.int32), 0)
+    assert e.value.status == -1
