@@ -1,0 +1,477 @@
+"""Benchmark: MLA decode throughput (achieved HBM GB/s, µs per call) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one mla_decode call (stage 1 + split reduce) over the workload's
+whole batch. Default workload: fp8, B=64, kv_len=8192 (16 q heads / 1 latent
+KV head, 576/512 dims, page_size 1): the bandwidth-bound headline, 304 MB of
+algorithmic traffic per call. Inputs are synthetic (seeded N(0,1)); two copies
+rotate so no call finds the previous call's rows in L2 (each copy is larger
+than the 129 MB L2). Timing: K decode calls captured in CUDA graphs, bracketed
+by a barrier, a device synchronise and CUDA events; max over ranks. Under
+torchrun every rank runs an independent replica (weak scaling, no collective
+on the data path).
+
+--impl reference times the float64 CPU oracle (the only reference this method
+has here) on the host cores, one bounded sample of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import mla_inputs as mi  # noqa: E402
+
+PROFILES = os.path.join(ROOT, "profiles")
+METRIC = "MLA decode achieved HBM GB/s (KV + Q + O bytes per call / time)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks (NVML, read only)
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons of one GPU in a thread (NVML via ctypes)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting",
+               0x1: "gpu_idle", 0x10: "sync_boost", 0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.error = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.handle = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device_index)
+            ok = False
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                key = str(uuid)
+                key = key if key.startswith("GPU-") else "GPU-" + key
+                ok = self.nvml.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.handle)) == 0
+            if not ok:
+                idx = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(device_index)).split(",")[device_index])
+                if self.nvml.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.handle)) != 0:
+                    raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+        except Exception as e:  # NVML missing: report no clocks rather than fail the benchmark
+            self.nvml = None
+            self.error = str(e)
+
+    def _read(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk))
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(self.handle, ctypes.byref(rs))
+        return int(clk.value), int(rs.value)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._read())
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            try:
+                self.samples.append(self._read())
+            except Exception:
+                pass
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml", "note": self.error or "no samples"}
+        mhz = [s[0] for s in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = [name for bit, name in self.REASONS.items() if mask & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(mhz), "source": "nvml"}
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stage1_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_decode_attention_09_gb300", "csrc")
+    for f in ("stage1.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per stage-1 launch from the committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(PROFILES, f"stage1_{workload}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha") != stage1_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def oracle_sample(w: mi.Workload, inp: mi.Inputs, n_seq: int):
+    """Time the float64 oracle on the first n_seq sequences; returns (seconds, bytes, threads)."""
+    import oracle
+    lib = oracle.load()
+    ids = list(range(min(n_seq, inp.batch)))
+    lens = inp.lengths()
+    row_bytes = inp.kv_row_bytes
+    nbytes = sum(int(lens[i]) * row_bytes for i in ids) + len(ids) * 16 * (576 + 512) * 2
+    t0 = time.perf_counter()
+    oracle.decode(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, inp.sm_scale, inp.mode, inp.kv_scale,
+                  seq_ids=ids, lib=lib)
+    return time.perf_counter() - t0, nbytes, oracle.threads(lib)
+
+
+# ---------------------------------------------------------------- our arm
+
+def bench_ours(args):
+    import mla_decode_attention_09_gb300 as mla
+    from mla_decode_attention_09_gb300 import build as mla_build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(ws, "nccl")
+    dev = torch.device("cuda", local)
+    mla_build.build()
+    w = mi.WORKLOADS[args.workload]
+    nbytes = mi.workload_bytes(w)
+    step_bytes = nbytes["total"]
+
+    # two input copies, each larger than L2 for the headline workload (seeded per rank: independent replicas)
+    devs = [mi.make_workload(w, device=str(dev), seed_offset=1000 * rank + k) for k in range(2)]
+    scales = [d.kv_scale_tensor(dev) for d in devs]
+    plan = mla.plan(devs[0].kv_indptr.cpu(), 0, num_kv_slots=devs[0].kv.shape[0])
+    info = plan.info()
+    outs = [torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+
+    def call(k, stream=None):
+        d = devs[k]
+        mla.decode(d.q, d.kv, scales[k], d.kv_indptr, d.kv_indices, outs[k], sm_scale=d.sm_scale,
+                   dtype_mode=w.mode, plan=plan, stream=stream, validate=False)
+
+    for k in range(max(args.warmup, 3)):
+        call(k % 2)
+    torch.cuda.synchronize()
+    status = plan.check_error()
+    if status != 0:
+        raise RuntimeError(f"kernel error status {status}")
+
+    # CUDA graph with `chunk` decode calls (alternating copies), replayed to cover K steps
+    chunk = min(args.steps, 64)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for k in range(chunk):
+                call(k % 2)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    reps, tail = divmod(args.steps, chunk)
+    g_tail = None
+    if tail:
+        g_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g_tail, stream=s):
+                for k in range(tail):
+                    call(k % 2)
+        torch.cuda.current_stream().wait_stream(s)
+        g_tail.replay()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    if g_tail is not None:
+        g_tail.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sampler.stop()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, ws, dev)
+    status = plan.check_error()
+    if status != 0:
+        raise RuntimeError(f"kernel error status {status}")
+    ms_per_step = ms_max / args.steps
+    value = step_bytes * args.steps * ws / (ms_max * 1e-3) / 1e9
+    launches_per_step = 1 + (1 if info["num_split_seqs"] > 0 else 0)
+
+    # roofline of the dominant kernel: stage 1 alone, each launch bracketed by events on its stream
+    n_roof = max(8, min(args.steps, 200))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_roof)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)  # keep the GPU busy while the launches below are queued: no host gaps
+    for i in range(n_roof):
+        d = devs[i % 2]
+        ev[i][0].record()
+        mla.decode_stage1(d.q, d.kv, scales[i % 2], d.kv_indptr, d.kv_indices, outs[i % 2], plan=plan,
+                          sm_scale=d.sm_scale, dtype_mode=w.mode)
+        ev[i][1].record()
+        mla.decode_reduce(outs[i % 2], plan=plan)
+    torch.cuda.synchronize()
+    stage1_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    peak, peak_kind = measured_peak()
+    achieved = step_bytes / (stage1_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                "kernel": "mla_stage1_kernel", "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": step_bytes, "stage1_us": round(stage1_ms * 1e3, 2)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes)
+    assert plan.check_error() == 0
+    host0 = devs[0].to("cpu") if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+
+    cpu = None
+    if host0 is not None:
+        n_seq = args.cpu_sample_seqs
+        secs, cbytes, threads = oracle_sample(w, host0, n_seq)
+        cpu = {"value": round(cbytes / secs / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"float64 oracle on {min(n_seq, w.batch)} of {w.batch} sequences ({secs:.1f} s)"}
+
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "us_per_call": round(ms_per_step * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if w.mode == mi.MODE_FP8 else "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
+                   "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": 1, "bytes_per_call": step_bytes,
+                   "l2": "inputs larger than L2, two copies alternate", "timing": "CUDA graphs of decode calls",
+                   "plan": {k: info[k] for k in ("num_ctas", "num_work_items", "num_split_seqs")}},
+        "frac_of_peak": round(value / ws / peak, 4), "peak_gbs": peak,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if args.all_workloads and rank == 0:
+        line["per_workload"] = per_workload(mla, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes):
+    """End to end through the public API from pinned host buffers: H2D inputs, decode, D2H output."""
+    host0 = devs[0].to("cpu")
+    pinned = [{"q": host0.q.pin_memory(), "kv": host0.kv.pin_memory(), "ip": host0.kv_indptr.pin_memory(),
+               "ix": host0.kv_indices.pin_memory(),
+               "ks": torch.tensor([host0.kv_scale], dtype=torch.float32).pin_memory()}]
+    out_host = torch.empty((w.batch, 16, 512), dtype=torch.bfloat16).pin_memory()
+    d = devs[0]
+    h2d = sum(t.numel() * t.element_size() for t in pinned[0].values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        p = pinned[0]
+        d.q.copy_(p["q"], non_blocking=True)
+        d.kv.copy_(p["kv"], non_blocking=True)
+        d.kv_indptr.copy_(p["ip"], non_blocking=True)
+        d.kv_indices.copy_(p["ix"], non_blocking=True)
+        scales[0].copy_(p["ks"], non_blocking=True)
+        mla.decode(d.q, d.kv, scales[0], d.kv_indptr, d.kv_indices, outs[0], sm_scale=d.sm_scale,
+                   dtype_mode=w.mode, plan=plan, validate=False)
+        out_host.copy_(outs[0], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    t1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev) / e2e_steps
+    e2e = {"value": round(step_bytes * ws / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+           "note": "all inputs (q, KV cache, indices, scale) copied from pinned host memory every step"}
+    return e2e
+
+
+def per_workload(mla, dev, calls: int = 200):
+    """µs/call and GB/s of every workload (cold L2: a scrub write between timed calls)."""
+    res = {}
+    scrub = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for name, w in mi.WORKLOADS.items():
+        inp = mi.make_workload(w, device=str(dev))
+        ks = inp.kv_scale_tensor(dev)
+        plan = mla.plan(inp.kv_indptr.cpu(), 0, num_kv_slots=inp.kv.shape[0])
+        out = torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev)
+        torch.cuda._sleep(100_000_000)
+        for _ in range(5):
+            mla.decode(inp.q, inp.kv, ks, inp.kv_indptr, inp.kv_indices, out, sm_scale=inp.sm_scale,
+                       dtype_mode=w.mode, plan=plan, validate=False)
+        times = []
+        for _ in range(calls):
+            scrub.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            mla.decode(inp.q, inp.kv, ks, inp.kv_indptr, inp.kv_indices, out, sm_scale=inp.sm_scale,
+                       dtype_mode=w.mode, plan=plan, validate=False)
+            b.record()
+            times.append((a, b))
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
+        nb = mi.workload_bytes(w)["total"]
+        res[name] = {"us_per_call": round(us, 2), "gbs": round(nb / (us * 1e-6) / 1e9, 1),
+                     "bytes": nb, "l2": "cold (512 MB scrub write before each call)"}
+        assert plan.check_error() == 0
+        del inp, out, plan
+    return res
+
+
+# ---------------------------------------------------------------- reference arm (the oracle on host cores)
+
+def bench_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = mi.WORKLOADS[args.workload]
+    host = mi.make_workload(w)
+    lib = oracle.load()
+    lens = host.lengths()
+    # each step: the oracle over a bounded run of one sequence's rows, sized so K steps stay within minutes
+    rows = int(max(64, min(int(lens.max()), 8192 * 50 // max(args.steps, 1))))
+    row_bytes = host.kv_row_bytes
+
+    def one(step):
+        b = step % w.batch
+        n = min(rows, int(lens[b]))
+        t0 = time.perf_counter()
+        oracle.decode_range(host.q, host.kv, host.kv_indptr, host.kv_indices, host.sm_scale, b, 0, n,
+                            host.mode, host.kv_scale, lib=lib)
+        return time.perf_counter() - t0, n * row_bytes + 16 * (576 + 512) * 2
+
+    for i in range(args.warmup):
+        one(i)
+    t_total, b_total = 0.0, 0
+    for i in range(args.steps):
+        secs, nb = one(i)
+        t_total += secs
+        b_total += nb
+    value = b_total / t_total / 1e9
+    threads = oracle.threads(lib)
+    sample = f"float64 oracle over the first {rows} rows of one sequence per step (all 16 heads)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch},
+        "cpu_baseline": {"kind": "oracle", "cores": threads, "value": round(value, 5), "unit": UNIT,
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="fp8_b64_l8192", choices=list(mi.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--all-workloads", action="store_true", help="add µs/call of every workload to the line")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-seqs", type=int, default=8)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()
