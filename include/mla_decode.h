@@ -68,7 +68,8 @@ enum mla_status {
   MLA_ERR_NOMEM = -7,         /* device or host allocation failed while planning */
   MLA_ERR_INDEX = -8,         /* a kv_indices entry lies outside [0, num_kv_slots) (reported by the kernel) */
   MLA_ERR_DEVICE = -9,        /* no usable sm_103 device, or the plan belongs to another device */
-  MLA_ERR_INDPTR = -10        /* host kv_indptr not non-decreasing from 0, or a sequence too long */
+  MLA_ERR_INDPTR = -10,       /* host kv_indptr not non-decreasing from 0, or a sequence too long */
+  MLA_ERR_NOALLOC_LIMIT = -11 /* mla_decode_noalloc: the request needs more than its fixed scratch holds */
 };
 
 /* Opaque plan: split-KV work list, reduce map and the partial-result
@@ -199,6 +200,47 @@ int mla_plan_check_error(mla_plan* plan, void* stream);
 int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
                           int32_t* counts, int32_t* items, int items_cap, int32_t* work_indptr, int indptr_cap,
                           int32_t* reduce, int reduce_cap);
+
+/*
+ * mla_decode_noalloc — the same decode as mla_decode, for callers that cannot
+ * allocate device memory. The paper has no counterpart of this entry point.
+ *
+ * Who needs it: code that is handed a stream and its buffers but may not call
+ * cudaMalloc — for example a plug-in inside a framework whose caching
+ * allocator has already reserved the device's memory, or a latency-critical
+ * serving loop that cannot accept cudaMalloc's implicit device
+ * synchronisation. Such a caller cannot build an mla_plan (mla_decode_plan
+ * allocates the plan's workspace). This call instead plans on the host into
+ * stack arrays and keeps the work list and the fp32 partial results in one
+ * fixed array of device memory inside the library: 16 MiB, present on every
+ * GPU that loads the library until the process exits. It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Limits: batch <= 1024 sequences and at most 500 partial results of split
+ * sequences per call (the split targets one chunk per SM, so a split sequence
+ * usually needs two or three). Larger requests return MLA_ERR_NOALLOC_LIMIT
+ * before any device work is queued.
+ *
+ * Arguments as for mla_decode, plus:
+ *   kv_indptr_host host int32 [batch+1]: the same offsets as the device kv_indptr
+ *                  (the split is planned from it on every call).
+ *   batch          number of sequences.
+ *   num_kv_slots   rows in the KV pool; kv_indices are checked against it in the
+ *                  kernel (0 = unchecked).
+ *   status_dev     device int owned by the caller. This call sets it to 0 on the
+ *                  stream; the kernels then record the first error they detect
+ *                  (MLA_ERR_TIMEOUT, MLA_ERR_PLAN_MISMATCH, MLA_ERR_INDEX).
+ * The first call on a device does a one-time set-up: it resolves the array's
+ * device address and clears part of it, and synchronises the device. Make that
+ * first call before any stream capture. Every call reuses the same array, which
+ * keeps the last call's contents: calls whose device work overlaps (on
+ * different streams, or unordered) race on it and corrupt each other's results.
+ * Errors returned directly: MLA_ERR_ARG, MLA_ERR_DTYPE, MLA_ERR_ALIGN,
+ * MLA_ERR_INDPTR, MLA_ERR_DEVICE, MLA_ERR_CUDA, MLA_ERR_NOALLOC_LIMIT.
+ */
+int mla_decode_noalloc(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr_host,
+                       const int32_t* kv_indptr, const int32_t* kv_indices, int batch, int64_t num_kv_slots,
+                       void* out, float sm_scale, int dtype_mode, int* status_dev, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* mla_strerror(int status);

@@ -33,14 +33,14 @@ MLA_OK = 0
 STATUS = {
     0: "MLA_OK", -1: "MLA_ERR_ARG", -2: "MLA_ERR_DTYPE", -3: "MLA_ERR_PLAN_MISMATCH", -4: "MLA_ERR_CUDA",
     -5: "MLA_ERR_TIMEOUT", -6: "MLA_ERR_ALIGN", -7: "MLA_ERR_NOMEM", -8: "MLA_ERR_INDEX", -9: "MLA_ERR_DEVICE",
-    -10: "MLA_ERR_INDPTR",
+    -10: "MLA_ERR_INDPTR", -11: "MLA_ERR_NOALLOC_LIMIT",
 }
 
 # Every symbol include/mla_decode.h declares.
 EXPORTS = (
     "mla_decode_plan", "mla_decode_plan_ex", "mla_plan_release", "mla_plan_get_info", "mla_decode",
     "mla_decode_stage1", "mla_decode_reduce", "mla_plan_check_error", "mla_strerror", "mla_version",
-    "mla_plan_compute_host",
+    "mla_plan_compute_host", "mla_decode_noalloc",
 )
 
 
@@ -93,6 +93,7 @@ def load_library(path: str | None = None):
         lib.mla_strerror.restype = ctypes.c_char_p
         lib.mla_version.argtypes = []
         lib.mla_plan_compute_host.argtypes = [I, V, I, ctypes.POINTER(PlanOptions), V, V, I, V, I, V, I]
+        lib.mla_decode_noalloc.argtypes = [V, V, V, V, V, V, I, I64, V, F, I, V, V]
         for name in EXPORTS:
             if name not in ("mla_strerror",):
                 getattr(lib, name).restype = I

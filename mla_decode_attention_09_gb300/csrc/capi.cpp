@@ -270,6 +270,8 @@ const char* mla_strerror(int status) {
     case MLA_ERR_INDEX: return "kv_indices entry out of range";
     case MLA_ERR_DEVICE: return "no usable sm_103 device or wrong device for the plan";
     case MLA_ERR_INDPTR: return "kv_indptr must start at 0 and be non-decreasing";
+    case MLA_ERR_NOALLOC_LIMIT:
+      return "request exceeds the fixed scratch of mla_decode_noalloc (batch <= 1024, <= 500 partial slots)";
     default: return "unknown status";
   }
 }
