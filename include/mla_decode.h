@@ -84,6 +84,8 @@ typedef struct mla_plan_options {
   int min_rows_per_split; /* smallest KV chunk the planner cuts (default 256) */
   int granularity;        /* chunk boundaries are multiples of this many rows (default 16) */
   int ctas_per_sm;        /* persistent CTAs per SM (default 1) */
+  int fp8_kernel;         /* fp8 stage-1 kernel: 0 = 5th-generation tensor cores (tcgen05 + TMA, default),
+                             1 = warp-level mma.sync (kept for comparison) */
 } mla_plan_options;
 
 /* Read-only description of a plan. */

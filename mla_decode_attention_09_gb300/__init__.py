@@ -52,7 +52,7 @@ class MLAError(RuntimeError):
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("num_kv_slots", ctypes.c_int64), ("min_rows_per_split", ctypes.c_int),
-                ("granularity", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
+                ("granularity", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("fp8_kernel", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -114,8 +114,9 @@ def _check(status: int, what: str):
         raise MLAError(status, what)
 
 
-def _opts(num_kv_slots=0, min_rows_per_split=0, granularity=0, ctas_per_sm=0) -> PlanOptions:
-    return PlanOptions(int(num_kv_slots), int(min_rows_per_split), int(granularity), int(ctas_per_sm))
+def _opts(num_kv_slots=0, min_rows_per_split=0, granularity=0, ctas_per_sm=0, fp8_kernel=0) -> PlanOptions:
+    return PlanOptions(int(num_kv_slots), int(min_rows_per_split), int(granularity), int(ctas_per_sm),
+                       int(fp8_kernel))
 
 
 def _host_indptr(kv_indptr) -> torch.Tensor:

@@ -37,6 +37,7 @@ bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, i
   return p->device == device && p->batch == batch && p->num_sms == num_sms &&
          p->opt.num_kv_slots == o.num_kv_slots && p->opt.min_rows_per_split == o.min_rows_per_split &&
          p->opt.granularity == o.granularity && p->opt.ctas_per_sm == o.ctas_per_sm &&
+         p->opt.fp8_kernel == o.fp8_kernel &&
          std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0;
 }
 
@@ -122,6 +123,7 @@ int make_plan(int batch, const int32_t* kv_indptr_host, int num_sms, const mla::
   p->dev.num_kv_slots = opt.num_kv_slots;
   p->dev.num_ctas = h.num_ctas;
   p->dev.n_reduce = h.n_reduce;
+  p->dev.fp8_kernel = opt.fp8_kernel;
   p->zero_row = base + o_zero;
   p->refcount = 1;
   *out = p;

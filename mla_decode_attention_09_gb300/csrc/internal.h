@@ -56,6 +56,7 @@ struct PlanOptions {
   int min_rows_per_split = 256;
   int granularity = 16;
   int ctas_per_sm = 1;
+  int fp8_kernel = 0;  // 0 = tcgen05 / TMA kernel, 1 = warp-level mma.sync kernel
 };
 
 PlanOptions resolve_options(const mla_plan_options* o);
@@ -76,6 +77,7 @@ struct DevicePlan {
   int64_t num_kv_slots;  // 0 = unchecked
   int num_ctas;
   int n_reduce;
+  int fp8_kernel;        // see PlanOptions
 };
 
 struct DecodeArgs {
@@ -91,5 +93,6 @@ struct DecodeArgs {
 // Kernel launchers (stage1.cu / reduce.cu). Return cudaError_t as int.
 int launch_stage1(int dtype_mode, const DecodeArgs& a, const DevicePlan& p, const void* zero_row, void* stream);
 int launch_reduce(void* out, const DevicePlan& p, void* stream, bool pdl);
+int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* stream);
 
 }  // namespace mla

@@ -29,6 +29,7 @@ PlanOptions resolve_options(const mla_plan_options* o) {
   if (o->min_rows_per_split > 0) r.min_rows_per_split = o->min_rows_per_split;
   if (o->granularity > 0) r.granularity = o->granularity;
   if (o->ctas_per_sm > 0) r.ctas_per_sm = o->ctas_per_sm;
+  if (o->fp8_kernel == 1) r.fp8_kernel = 1;
   return r;
 }
 
