@@ -218,7 +218,7 @@ def bench_ours(args):
     # two input copies, each larger than L2 for the headline workload (seeded per rank: independent replicas)
     devs = [mi.make_workload(w, device=str(dev), seed_offset=1000 * rank + k) for k in range(2)]
     scales = [d.kv_scale_tensor(dev) for d in devs]
-    plan = mla.plan(devs[0].kv_indptr.cpu(), 0, num_kv_slots=devs[0].kv.shape[0])
+    plan = mla.plan(devs[0].kv_indptr.cpu(), 0, num_kv_slots=devs[0].kv.shape[0], fp8_kernel=args.fp8_kernel)
     info = plan.info()
     outs = [torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(2)]
 
@@ -299,7 +299,8 @@ def bench_ours(args):
     achieved = step_bytes / (stage1_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
-                "kernel": "mla_stage1_kernel", "peak_kind": peak_kind,
+                "kernel": ("mla_stage1_fp8_umma_kernel" if (w.mode == mi.MODE_FP8 and args.fp8_kernel == 0)
+                           else "mla_stage1_kernel"), "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": step_bytes, "stage1_us": round(stage1_ms * 1e3, 2)}
 
     e2e = None
@@ -324,13 +325,14 @@ def bench_ours(args):
         "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
                    "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": 1, "bytes_per_call": step_bytes,
                    "l2": "inputs larger than L2, two copies alternate", "timing": "CUDA graphs of decode calls",
-                   "plan": {k: info[k] for k in ("num_ctas", "num_work_items", "num_split_seqs")}},
+                   "plan": {k: info[k] for k in ("num_ctas", "num_work_items", "num_split_seqs")},
+                   "fp8_kernel": ("tcgen05" if args.fp8_kernel == 0 else "mma.sync") if w.mode == mi.MODE_FP8 else None},
         "frac_of_peak": round(value / ws / peak, 4), "peak_gbs": peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
     if args.all_workloads and rank == 0:
-        line["per_workload"] = per_workload(mla, dev)
+        line["per_workload"] = per_workload(mla, dev, fp8_kernel=args.fp8_kernel)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -378,14 +380,14 @@ def bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes):
     return e2e
 
 
-def per_workload(mla, dev, calls: int = 200):
+def per_workload(mla, dev, calls: int = 200, fp8_kernel: int = 0):
     """µs/call and GB/s of every workload (cold L2: a scrub write between timed calls)."""
     res = {}
     scrub = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for name, w in mi.WORKLOADS.items():
         inp = mi.make_workload(w, device=str(dev))
         ks = inp.kv_scale_tensor(dev)
-        plan = mla.plan(inp.kv_indptr.cpu(), 0, num_kv_slots=inp.kv.shape[0])
+        plan = mla.plan(inp.kv_indptr.cpu(), 0, num_kv_slots=inp.kv.shape[0], fp8_kernel=fp8_kernel)
         out = torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev)
         torch.cuda._sleep(100_000_000)
         for _ in range(5):
@@ -465,6 +467,8 @@ def main():
     ap.add_argument("--all-workloads", action="store_true", help="add µs/call of every workload to the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8-kernel", type=int, default=0, choices=[0, 1],
+                    help="fp8 stage-1 kernel: 0 tcgen05/TMA (default), 1 warp-level mma.sync")
     ap.add_argument("--cpu-sample-seqs", type=int, default=8)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -6,14 +6,15 @@
 //
 // Per 128-row KV tile (rows = tokens of one sequence):
 //   S^T[128 tokens x 16 heads] = K_tile[128 x 576] . Q^T[576 x 16]
-//       tcgen05.mma kind::f8f6f4, M = 128 tokens, N = 16 heads, K = 32 x 18,
-//       A = the KV tile (K-major, 128-byte swizzled, straight from TMA),
-//       B = the e4m3 query (K-major, 128-byte swizzled), D in TMEM.
+//       tcgen05.mma kind::f8f6f4, M = 128 tokens, N = 16 heads, 18 steps of
+//       K = 32: A = the KV tile (K-major; latent part 128-byte swizzled, rope
+//       part 64-byte swizzled, both straight from TMA), B = the e4m3 query
+//       (same layouts), D in TMEM.
 //   softmax over tokens per head (4 warps, one thread per token row),
 //   P^T written to shared memory as [token][16 heads] e4m3,
 //   O^T[512 dims x 16 heads] += V^T[512 x 128] . P^T[128 x 16]
-//       four M = 128 MMAs per 32-token k-step, A = the same KV tile read
-//       MN-major (dims contiguous), B = P^T MN-major, D in TMEM.
+//       four M = 128 MMAs per 32-token k-step, A = the latent part of the same
+//       tile read MN-major (dims contiguous), B = P^T MN-major, D in TMEM.
 // The value vectors are the first 512 entries of the rows used as keys
 // (kernelbot amd-mixed-mla submission 689529 "MLA decode V3", custom_kernel
 // passes one KV buffer for both), the query is cast directly to e4m3 with
@@ -22,15 +23,19 @@
 //
 // Warp roles (192 threads): warps 0-3 softmax and epilogue (warp w reads TMEM
 // lanes 32w..32w+31), warp 4 TMA producer and query staging, warp 5 TMEM
-// allocation and the single MMA-issuing thread. Two KV stages of 80 KB,
-// double-buffered S, P, Q and O. The running max per head is updated lazily:
+// allocation and the single MMA-issuing thread. The latent part of a tile
+// (512 B per row, needed until P.V finishes) lives in a 3-slot ring of 64 KB,
+// the rope part (64 B per row, needed only by the scores) in a 2-slot ring of
+// 8 KB, so three tiles can be resident or in flight. S, P and O are double
+// buffered. The producer and the MMA thread poll their barriers and never
+// block one activity on another. The running max per head is updated lazily:
 // O in TMEM is rescaled only when a tile's max exceeds the reference by more
 // than 2^8, so P = 2^(s - m_ref) <= 256 stays inside e4m3's range.
 //
-// KV rows arrive by TMA: a tile whose 128 row indices are consecutive is
-// five 2-D box loads (128 rows x 128 bytes each); any other tile uses 4-row
-// gather loads. Rows past the end of an item, and rows whose index is out of
-// range, are read at an out-of-bounds coordinate, which TMA fills with zeros.
+// KV rows arrive by TMA: a tile whose 128 row indices are consecutive is five
+// 2-D box loads; any other tile uses 4-row gather loads. Rows past the end of
+// an item, and rows whose index is out of range, are read at an out-of-bounds
+// coordinate, which TMA fills with zeros.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -46,40 +51,57 @@
 namespace mla {
 namespace {
 
-constexpr int kRowsU = 128;                 // KV rows per tile = UMMA M of the scores
-constexpr int kCB = 5;                      // 128-byte column blocks per row (576 B = 4.5 blocks)
-constexpr int kBlk = kRowsU * 128;          // 16 KB per column block
-constexpr int kStageU = kCB * kBlk;         // 80 KB per KV stage
-constexpr int kQBuf = kCB * 16 * 128;       // 10 KB: e4m3 query, 5 K-blocks x 16 heads x 128 B
-constexpr int kPBuf = kRowsU * 16;          // 2 KB: P^T [128 tokens][16 heads] e4m3
+constexpr int kRowsU = 128;                   // KV rows per tile = UMMA M of the scores
+constexpr int kBlk = kRowsU * 128;            // 16 KB: one 128-byte column block of a tile
+constexpr int kLatStage = 4 * kBlk;           // 64 KB: latent / value part (4 column blocks)
+constexpr int kRopeStage = kRowsU * 64;       // 8 KB: rope part (64-byte rows)
+constexpr int kLatStages = 3, kRopeStages = 2;
+constexpr int kQLat = 4 * 16 * 128;           // 8 KB: e4m3 query latent part, 4 K-blocks x 16 heads x 128 B
+constexpr int kQBytes = kQLat + 16 * 64;      // + 1 KB rope part
+constexpr int kPBuf = kRowsU * 16;            // 2 KB: P^T [128 tokens][16 heads] e4m3
+constexpr uint32_t kTileTx = kLatStage + kRopeStage;
 constexpr int kThreadsU = 192;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;               // S^T: 2 buffers x 16 columns
-constexpr uint32_t kColO = 32;              // O^T: 2 buffers x 4 blocks x 16 columns
+constexpr uint32_t kColS = 0;                 // S^T: 2 buffers x 16 columns
+constexpr uint32_t kColO = 32;                // O^T: 2 buffers x 4 blocks x 16 columns
 constexpr float kTau = 8.0f;
 constexpr uint64_t kWaitLimitNsU = 2000000000ull;
 constexpr uint64_t kDrainLimitNsU = 200000000ull;
 constexpr float kLog2eU = 1.4426950408889634f;
 constexpr uint32_t kIdescQK = umma::idesc_e4m3(128, 16, 0, 0);
 constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 16, 1, 1);
+constexpr uint32_t kLayoutSw64 = 4;
+
+enum : int {
+  kBFull = 0,     // [3] tile data landed (TMA tx)
+  kBLEmpty = 3,   // [3] latent slot free (P.V done)
+  kBREmpty = 6,   // [2] rope slot free (scores done)
+  kBSFull = 8,    // [2] S^T ready
+  kBPFull = 10,   // [2] P^T written (128 arrivals)
+  kBPEmpty = 12,  // [2] P^T consumed (P.V done)
+  kBQFull = 14,   // query staged (32 arrivals)
+  kBQEmpty = 15,  // query consumed (last scores of the item done)
+  kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals)
+  kBDrain = 18,   // every MMA of the CTA done
+  kNumBars = 19
+};
 
 struct SU {
-  static constexpr int kStage = 0;                   // 2 x 80 KB, 1024-aligned
-  static constexpr int kQ = 2 * kStageU;             // 2 x 10 KB
-  static constexpr int kP = kQ + 2 * kQBuf;          // 2 x 2 KB
-  static constexpr int kRed = kP + 2 * kPBuf;        // [2][16 heads][4 warps] fp32 tile max
-  static constexpr int kLsum = kRed + 2 * 64 * 4;    // [16 heads][4 warps] fp32 row sums
-  static constexpr int kBar = kLsum + 64 * 4;        // 17 mbarriers
-  static constexpr int kTmemSlot = kBar + 17 * 8;
+  static constexpr int kLat = 0;                                // 3 x 64 KB
+  static constexpr int kRope = kLat + kLatStages * kLatStage;   // 2 x 8 KB
+  static constexpr int kQ = kRope + kRopeStages * kRopeStage;   // 9 KB
+  static constexpr int kP = kQ + kQBytes;                       // 2 x 2 KB
+  static constexpr int kRed = kP + 2 * kPBuf;                   // [2][16 heads][4 warps] fp32 tile max
+  static constexpr int kLsum = kRed + 2 * 64 * 4;               // [16 heads][4 warps] fp32 row sums
+  static constexpr int kBar = kLsum + 64 * 4;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
-  static constexpr int kAlloc = kBytes + 1024;       // base is rounded up to 1024 inside the kernel
+  static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 inside the kernel
 };
 static_assert(SU::kAlloc <= 232448, "tcgen05 stage-1 shared memory");
-enum : int {
-  kBFull = 0, kBEmpty = 2, kBSFull = 4, kBPFull = 6, kBPEmpty = 8, kBQFull = 10, kBQEmpty = 12, kBOEmpty = 14,
-  kBDrain = 16
-};
+static_assert(SU::kQ % 1024 == 0 && SU::kRope % 1024 == 0 && SU::kP % 16 == 0 && SU::kBar % 8 == 0,
+              "operand alignment");
 
 __device__ __forceinline__ void record_error_u(int* err, int code) { atomicCAS(err, 0, code); }
 
@@ -100,6 +122,24 @@ __device__ __forceinline__ bool wait_u(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
+
+// Idle bookkeeping of a polling loop: returns false once the loop has made no
+// progress for the wait limit, or another role aborted.
+struct IdleClock {
+  uint64_t since = 0;
+  __device__ __forceinline__ void reset() { since = 0; }
+  __device__ __forceinline__ bool tick(volatile int* abort_flag) {
+    __nanosleep(32);
+    const uint64_t now = ptx::globaltimer_ns();
+    if (since == 0) since = now;
+    if (*abort_flag) return false;
+    if (now - since > kWaitLimitNsU) {
+      *abort_flag = 1;
+      return false;
+    }
+    return true;
+  }
+};
 
 // Tile stream of one CTA (items without rows or with a mismatched length are skipped).
 struct TCur {
@@ -132,12 +172,20 @@ __device__ __forceinline__ void tcur_init(TCur& c, int it, int it_end, const Dev
   tcur_settle(c, p, ip);
 }
 __device__ __forceinline__ void tcur_next(TCur& c, const DevicePlan& p, const int32_t* ip) {
+  if (c.done) return;
   c.t0 += kRowsU;
   if (c.t0 >= c.t_end) {
     ++c.it;
     ++c.k;
     tcur_settle(c, p, ip);
   }
+}
+// Move to the first tile of the next item.
+__device__ __forceinline__ void tcur_next_item(TCur& c, const DevicePlan& p, const int32_t* ip) {
+  if (c.done) return;
+  ++c.it;
+  ++c.k;
+  tcur_settle(c, p, ip);
 }
 
 // Warp-wide transpose reduction of 16 per-lane values: returns, in every lane,
@@ -163,41 +211,55 @@ __device__ __forceinline__ uint32_t cast4_e4m3(uint32_t bf_lo, uint32_t bf_hi) {
   return ptx::f32x2_to_e4m3x2(f0, f1) | (ptx::f32x2_to_e4m3x2(f2, f3) << 16);
 }
 
+// Byte offset of query element (head h, dims d0..d0+7) in the staged query:
+// latent dims in 128-byte-swizzled K-blocks, rope dims in a 64-byte-swizzled block.
+__device__ __forceinline__ int q_offset(int h, int d0) {
+  const int r = h & 7;
+  if (d0 < 512) {
+    const int kb = d0 >> 7, x = d0 & 127;
+    return kb * 2048 + (h >> 3) * 1024 + r * 128 + (((x >> 4) ^ r) << 4) + (x & 8);
+  }
+  const int x = d0 - 512;
+  return kQLat + (h >> 3) * 512 + r * 64 + (((x >> 4) ^ ((r >> 1) & 3)) << 4) + (x & 8);
+}
+
+struct KvMaps {
+  CUtensorMap lat_tile, lat_gather, rope_tile, rope_gather;
+};
+
 __global__ void __launch_bounds__(kThreadsU, 1)
-    mla_stage1_fp8_umma_kernel(const DecodeArgs a, const DevicePlan p, const __grid_constant__ CUtensorMap tm_tile,
-                               const __grid_constant__ CUtensorMap tm_gather, const int32_t oob_row) {
+    mla_stage1_fp8_umma_kernel(const DecodeArgs a, const DevicePlan p, const __grid_constant__ KvMaps tm,
+                               const int32_t oob_row) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((int)blockIdx.x >= p.num_ctas) return;
   const int item_begin = p.work_indptr[blockIdx.x], item_end = p.work_indptr[blockIdx.x + 1];
 
-  // 1024-aligned base for the 128-byte swizzle atoms
+  // 1024-aligned base for the swizzle atoms
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const uint32_t stage_addr = base + SU::kStage, q_addr = base + SU::kQ, p_addr = base + SU::kP;
+  const uint32_t lat_addr = base + SU::kLat, rope_addr = base + SU::kRope, q_addr = base + SU::kQ;
+  const uint32_t p_addr = base + SU::kP;
   float* red = reinterpret_cast<float*>(smem + SU::kRed);
   float* lsum = reinterpret_cast<float*>(smem + SU::kLsum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SU::kAbort);
   auto bar = [&](int i) { return base + SU::kBar + 8u * (uint32_t)i; };
 
   if (tid == 0) {
-    ptx::mbar_init(bar(kBFull), 1);
-    ptx::mbar_init(bar(kBFull + 1), 1);
-    ptx::mbar_init(bar(kBEmpty), 1);
-    ptx::mbar_init(bar(kBEmpty + 1), 1);
-    ptx::mbar_init(bar(kBSFull), 1);
-    ptx::mbar_init(bar(kBSFull + 1), 1);
-    ptx::mbar_init(bar(kBPFull), 128);
-    ptx::mbar_init(bar(kBPFull + 1), 128);
-    ptx::mbar_init(bar(kBPEmpty), 1);
-    ptx::mbar_init(bar(kBPEmpty + 1), 1);
+    for (int i = 0; i < 3; ++i) {
+      ptx::mbar_init(bar(kBFull + i), 1);
+      ptx::mbar_init(bar(kBLEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(kBREmpty + i), 1);
+      ptx::mbar_init(bar(kBSFull + i), 1);
+      ptx::mbar_init(bar(kBPFull + i), 128);
+      ptx::mbar_init(bar(kBPEmpty + i), 1);
+      ptx::mbar_init(bar(kBOEmpty + i), 128);
+    }
     ptx::mbar_init(bar(kBQFull), 32);
-    ptx::mbar_init(bar(kBQFull + 1), 32);
     ptx::mbar_init(bar(kBQEmpty), 1);
-    ptx::mbar_init(bar(kBQEmpty + 1), 1);
-    ptx::mbar_init(bar(kBOEmpty), 128);
-    ptx::mbar_init(bar(kBOEmpty + 1), 128);
     ptx::mbar_init(bar(kBDrain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -216,49 +278,23 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const float score_log2 = a.sm_scale * kv_scale * kLog2eU;
 
   if (warp == 4) {
-    // ------------------------------------------------ producer: query staging + KV tiles
+    // ------------------------------------------------ producer: KV tiles + query staging
     if (lane == 0) {
-      umma::tma_prefetch_desc(&tm_tile);
-      umma::tma_prefetch_desc(&tm_gather);
+      umma::tma_prefetch_desc(&tm.lat_tile);
+      umma::tma_prefetch_desc(&tm.lat_gather);
+      umma::tma_prefetch_desc(&tm.rope_tile);
+      umma::tma_prefetch_desc(&tm.rope_gather);
     }
     const uint64_t pol = ptx::l2_evict_first_policy();
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    TCur c;
-    tcur_init(c, item_begin, item_end, p, a.kv_indptr);
-    int i = 0, q_item = -1;
-    bool ok = true;
-    while (!c.done && ok) {
-      if (c.k != q_item) {  // first tile of an item: stage its e4m3 query (K-major, 128-byte swizzle)
-        if (c.k >= 2 && !wait_u(bar(kBQEmpty + (c.k & 1)), ((c.k >> 1) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const __nv_bfloat16* qb = q + (int64_t)c.b * kHeads * kQkDim;
-        uint8_t* qs = smem + SU::kQ + (c.k & 1) * kQBuf;
-        for (int ci = lane; ci < kHeads * 72; ci += 32) {
-          const int h = ci / 72, d0 = (ci % 72) * 8;
-          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + h * kQkDim + d0));
-          const int kb = d0 >> 7, x = d0 & 127, r = h & 7;
-          uint8_t* dst = qs + kb * 2048 + (h >> 3) * 1024 + r * 128 + ((((x >> 4) ^ r)) << 4) + (x & 8);
-          *reinterpret_cast<uint2*>(dst) = make_uint2(cast4_e4m3(raw.x, raw.y), cast4_e4m3(raw.z, raw.w));
-        }
-        umma::fence_proxy_async_smem();
-        umma::mbar_arrive(bar(kBQFull + (c.k & 1)));
-        q_item = c.k;
-      }
-      const int s = i & 1;
-      if (i >= 2 && !wait_u(bar(kBEmpty + s), ((i >> 1) - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const int nv = min(kRowsU, c.t_end - c.t0);
-      int y[4];
+    // row sources of one tile held by this lane: rows lane + 32 j (index loads run two tiles ahead)
+    auto load_rows = [&](const TCur& t, int (&y)[4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = lane + 32 * j;
         int v = oob_row;
-        if (r < nv) {
-          const int idx = __ldg(a.kv_indices + c.base + c.t0 + r);
+        if (!t.done && r < t.t_end - t.t0) {
+          const int idx = __ldg(a.kv_indices + t.base + t.t0 + r);
           if (idx >= 0 && (p.num_kv_slots == 0 || idx < p.num_kv_slots))
             v = idx;
           else
@@ -266,96 +302,187 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
         y[j] = v;
       }
-      const int y0 = __shfl_sync(~0u, y[0], 0);
-      bool contiguous = nv == kRowsU && y0 != oob_row;
+    };
+    // query of one item as e4m3, 8 bytes per chunk of 8 dims; lane holds chunks lane + 32 j
+    uint2 qr[36];
+    auto load_q = [&](int b) {
+      const __nv_bfloat16* qb = q + (int64_t)b * kHeads * kQkDim;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) contiguous = contiguous && (y[j] == y0 + lane + 32 * j);
-      contiguous = __all_sync(~0u, contiguous);
-      const uint32_t fb = bar(kBFull + s), dst = stage_addr + s * kStageU;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kStageU);
-      __syncwarp();
-      if (contiguous) {
-        if (lane < kCB) umma::tma_load_2d(dst + lane * kBlk, &tm_tile, lane * 128, y0, fb, pol);
-      } else {
-        // lane g gathers rows 4g..4g+3; row r is held by lane (r & 31), slot (r >> 5)
-        int ys[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int src = (4 * lane + jj) & 31;
-          const int v0 = __shfl_sync(~0u, y[0], src), v1 = __shfl_sync(~0u, y[1], src);
-          const int v2 = __shfl_sync(~0u, y[2], src), v3 = __shfl_sync(~0u, y[3], src);
-          const int slot = lane >> 3;
-          ys[jj] = slot == 0 ? v0 : (slot == 1 ? v1 : (slot == 2 ? v2 : v3));
-        }
-#pragma unroll
-        for (int cb = 0; cb < kCB; ++cb)
-          umma::tma_gather4(dst + cb * kBlk + lane * 512, &tm_gather, cb * 128, ys[0], ys[1], ys[2], ys[3], fb, pol);
+      for (int j = 0; j < 36; ++j) {
+        const int ci = lane + 32 * j, h = ci / 72, d0 = (ci % 72) * 8;
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qb + h * kQkDim + d0));
+        qr[j] = make_uint2(cast4_e4m3(raw.x, raw.y), cast4_e4m3(raw.z, raw.w));
       }
-      ++i;
-      tcur_next(c, p, a.kv_indptr);
+    };
+    auto store_q = [&]() {
+#pragma unroll
+      for (int j = 0; j < 36; ++j) {
+        const int ci = lane + 32 * j, h = ci / 72, d0 = (ci % 72) * 8;
+        *reinterpret_cast<uint2*>(smem + SU::kQ + q_offset(h, d0)) = qr[j];
+      }
+      umma::fence_proxy_async_smem();
+      umma::mbar_arrive(bar(kBQFull));
+    };
+
+    TCur c, c1, c2, qc;  // c: next tile to load; c1, c2: the two after; qc: item whose query is next
+    tcur_init(c, item_begin, item_end, p, a.kv_indptr);
+    c1 = c;
+    tcur_next(c1, p, a.kv_indptr);
+    c2 = c1;
+    tcur_next(c2, p, a.kv_indptr);
+    qc = c;
+    int y0s[4], y1s[4];
+    load_rows(c, y0s);
+    load_rows(c1, y1s);
+    if (!qc.done) load_q(qc.b);
+    int i = 0;
+    bool ok = true;
+    IdleClock idle;
+    while (!c.done || !qc.done) {
+      bool progress = false;
+      // query of item qc.k: the single buffer frees when the last scores of item qc.k - 1 complete
+      if (!qc.done) {
+        const bool free_ = qc.k == 0 || ptx::mbar_test_wait(bar(kBQEmpty), (qc.k - 1) & 1);
+        if (__shfl_sync(~0u, free_, 0)) {
+          store_q();
+          tcur_next_item(qc, p, a.kv_indptr);
+          if (!qc.done) load_q(qc.b);
+          progress = true;
+        }
+      }
+      if (!c.done) {
+        const int ls = i % kLatStages, rs = i & 1;
+        bool ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
+        ready = ready && (i < kRopeStages || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
+        if (__shfl_sync(~0u, ready, 0)) {
+          const int y0 = __shfl_sync(~0u, y0s[0], 0);
+          bool cont = (c.t_end - c.t0 >= kRowsU) && y0 != oob_row;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cont = cont && (y0s[j] == y0 + lane + 32 * j);
+          cont = __all_sync(~0u, cont);
+          const uint32_t fb = bar(kBFull + ls);
+          const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
+          if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kTileTx);
+          __syncwarp();
+          if (cont) {
+            if (lane < 4) umma::tma_load_2d(lat + lane * kBlk, &tm.lat_tile, lane * 128, y0, fb, pol);
+            if (lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
+          } else {
+            // lane g gathers rows 4g..4g+3; row r is held by lane (r & 31), slot (r >> 5)
+            int ys[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int src = (4 * lane + jj) & 31;
+              const int v0 = __shfl_sync(~0u, y0s[0], src), v1 = __shfl_sync(~0u, y0s[1], src);
+              const int v2 = __shfl_sync(~0u, y0s[2], src), v3 = __shfl_sync(~0u, y0s[3], src);
+              const int slot = lane >> 3;
+              ys[jj] = slot == 0 ? v0 : (slot == 1 ? v1 : (slot == 2 ? v2 : v3));
+            }
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb)
+              umma::tma_gather4(lat + cb * kBlk + lane * 512, &tm.lat_gather, cb * 128, ys[0], ys[1], ys[2], ys[3], fb,
+                                pol);
+            umma::tma_gather4(rope + lane * 256, &tm.rope_gather, 512, ys[0], ys[1], ys[2], ys[3], fb, pol);
+          }
+          // shift the index pipeline: tile i+1's indices are already loaded, request tile i+2's
+#pragma unroll
+          for (int j = 0; j < 4; ++j) y0s[j] = y1s[j];
+          load_rows(c2, y1s);
+          c = c1;
+          c1 = c2;
+          tcur_next(c2, p, a.kv_indptr);
+          ++i;
+          progress = true;
+        }
+      }
+      if (progress) {
+        idle.reset();
+      } else if (!idle.tick(abort_flag)) {
+        ok = false;
+        break;
+      }
     }
     if (!ok && lane == 0) record_error_u(p.err, MLA_ERR_TIMEOUT);
     // let issued loads land before the CTA can exit (they already have in the normal path)
-    for (int t = (i >= 2 ? i - 2 : 0); t < i; ++t) {
-      const uint32_t b_ = bar(kBFull + (t & 1));
-      if (ptx::mbar_try_wait(b_, (t >> 1) & 1)) continue;
-      (void)ptx::mbar_wait_bounded(b_, (t >> 1) & 1, kDrainLimitNsU);
+    for (int t = (i >= kLatStages ? i - kLatStages : 0); t < i; ++t) {
+      const uint32_t b_ = bar(kBFull + t % kLatStages);
+      const uint32_t par = (uint32_t)(t / kLatStages) & 1u;
+      if (ptx::mbar_try_wait(b_, par)) continue;
+      (void)ptx::mbar_wait_bounded(b_, par, kDrainLimitNsU);
     }
   } else if (warp == 5) {
     // ------------------------------------------------ MMA issue (one thread)
+    // P.V of tile j needs the softmax's P; scores of tile j need the tile's
+    // data (and, for an item's first tile, its query). Neither waits on the
+    // other: the thread polls both, P.V first (it frees a stage), and scores
+    // of tile j are allowed once P.V of tile j-2 is issued (two S buffers).
     if (lane == 0) {
       bool ok = true;
-      auto issue_qk = [&](const TCur& c, int i) -> bool {
-        const int s = i & 1;
-        if (c.t0 == c.t_begin && !wait_u(bar(kBQFull + (c.k & 1)), (c.k >> 1) & 1, abort_flag)) return false;
-        if (!wait_u(bar(kBFull + s), (i >> 1) & 1, abort_flag)) return false;
-        umma::fence_after_sync();
-        const uint32_t a0 = stage_addr + s * kStageU, b0 = q_addr + (c.k & 1) * kQBuf;
+      auto issue_qk = [&](const TCur& c, int i) {
+        const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
         const uint32_t d = tmem + kColS + 16u * (uint32_t)(i & 1);
-#pragma unroll
-        for (int st = 0; st < 18; ++st) {
-          const uint32_t kb = st >> 2, ko = (st & 3) * 32;
-          umma::mma_f8f6f4(d, umma::smem_desc(a0 + kb * kBlk + ko, 16, 1024, umma::kLayoutSw128),
-                           umma::smem_desc(b0 + kb * 2048 + ko, 16, 1024, umma::kLayoutSw128), kIdescQK, st > 0);
-        }
-        umma::commit(bar(kBSFull + (i & 1)));
-        return true;
-      };
-      auto issue_pv = [&](const TCur& d, int i) -> bool {
-        const int s = i & 1;
-        if (!wait_u(bar(kBPFull + (i & 1)), (i >> 1) & 1, abort_flag)) return false;
-        const bool first = d.t0 == d.t_begin;
-        if (first && d.k >= 2 && !wait_u(bar(kBOEmpty + (d.k & 1)), ((d.k >> 1) - 1) & 1, abort_flag)) return false;
         umma::fence_after_sync();
-        const uint32_t a0 = stage_addr + s * kStageU, p0 = p_addr + (i & 1) * kPBuf;
+#pragma unroll
+        for (int st = 0; st < 16; ++st) {
+          const uint32_t kb = st >> 2, ko = (st & 3) * 32;
+          umma::mma_f8f6f4(d, umma::smem_desc(lat + kb * kBlk + ko, 16, 1024, umma::kLayoutSw128),
+                           umma::smem_desc(q_addr + kb * 2048 + ko, 16, 1024, umma::kLayoutSw128), kIdescQK, st > 0);
+        }
+#pragma unroll
+        for (int st = 0; st < 2; ++st)
+          umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
+                           umma::smem_desc(q_addr + kQLat + st * 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
+        umma::commit(bar(kBSFull + (i & 1)));
+        umma::commit(bar(kBREmpty + (i & 1)));
+        if (c.t0 + kRowsU >= c.t_end) umma::commit(bar(kBQEmpty));
+      };
+      auto issue_pv = [&](const TCur& d, int i) {
+        const bool first = d.t0 == d.t_begin;
+        const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = p_addr + (i & 1) * kPBuf;
         const uint32_t ob = tmem + kColO + 64u * (uint32_t)(d.k & 1);
+        umma::fence_after_sync();
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            umma::mma_f8f6f4(ob + 16u * blk, umma::smem_desc(a0 + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
+            umma::mma_f8f6f4(ob + 16u * blk, umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
                              umma::smem_desc(p0 + j * 512, 128, 256, umma::kLayoutNone), kIdescPV,
                              (first && j == 0) ? 0u : 1u);
         umma::commit(bar(kBPEmpty + (i & 1)));
-        umma::commit(bar(kBEmpty + s));
-        if (d.t0 + kRowsU >= d.t_end) umma::commit(bar(kBQEmpty + (d.k & 1)));
-        return true;
+        umma::commit(bar(kBLEmpty + i % kLatStages));
       };
-      TCur c, d;
+      TCur c, d;  // c: next scores tile, d: next P.V tile
       tcur_init(c, item_begin, item_end, p, a.kv_indptr);
       d = c;
-      if (!c.done) {
-        ok = issue_qk(c, 0);
-        tcur_next(c, p, a.kv_indptr);
-      }
-      for (int t = 0; ok && !d.done; ++t) {
-        if (!c.done) {
-          ok = issue_qk(c, t + 1);
-          tcur_next(c, p, a.kv_indptr);
-          if (!ok) break;
+      int nq = 0, npv = 0;
+      IdleClock idle;
+      while (!d.done) {
+        bool progress = false;
+        if (npv < nq) {
+          const bool first = d.t0 == d.t_begin;
+          const bool oready = !first || d.k < 2 || ptx::mbar_test_wait(bar(kBOEmpty + (d.k & 1)), ((d.k >> 1) - 1) & 1);
+          if (oready && ptx::mbar_test_wait(bar(kBPFull + (npv & 1)), (npv >> 1) & 1)) {
+            issue_pv(d, npv);
+            ++npv;
+            tcur_next(d, p, a.kv_indptr);
+            progress = true;
+          }
         }
-        ok = issue_pv(d, t);
-        tcur_next(d, p, a.kv_indptr);
+        if (!c.done && nq <= npv + 1) {
+          const bool qready = c.t0 != c.t_begin || ptx::mbar_test_wait(bar(kBQFull), c.k & 1);
+          if (qready && ptx::mbar_test_wait(bar(kBFull + nq % kLatStages), (nq / kLatStages) & 1)) {
+            issue_qk(c, nq);
+            ++nq;
+            tcur_next(c, p, a.kv_indptr);
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle.reset();
+        } else if (!idle.tick(abort_flag)) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) record_error_u(p.err, MLA_ERR_TIMEOUT);
       // every MMA issued by this thread completes before TMEM is released
@@ -542,20 +669,31 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-int make_kv_maps(const void* kv, int64_t rows, CUtensorMap* tile, CUtensorMap* gather) {
+// Four views of the e4m3 KV pool [rows x 576 bytes]: latent part in 128-byte
+// boxes (128-byte swizzle) and rope part in 64-byte boxes (64-byte swizzle),
+// each as 128-row tiles and as single rows for 4-row gathers.
+int make_kv_maps(const void* kv, int64_t rows, KvMaps* m) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)kQkDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kQkDim};
-  const cuuint32_t box_t[2] = {128, (cuuint32_t)kRowsU}, box_g[2] = {128, 1}, es[2] = {1, 1};
+  const cuuint32_t es[2] = {1, 1};
   void* ptr = const_cast<void*>(kv);
-  if (enc(tile, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box_t, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-          CUDA_SUCCESS ||
-      enc(gather, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box_g, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-          CUDA_SUCCESS)
-    return (int)cudaErrorInvalidValue;
+  struct View {
+    CUtensorMap* map;
+    cuuint32_t w, h;
+    CUtensorMapSwizzle sw;
+  };
+  const View views[4] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
+                         {&m->lat_gather, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B},
+                         {&m->rope_tile, 64, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_64B},
+                         {&m->rope_gather, 64, 1, CU_TENSOR_MAP_SWIZZLE_64B}};
+  for (const View& v : views) {
+    const cuuint32_t box[2] = {v.w, v.h};
+    if (enc(v.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, v.sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return (int)cudaErrorInvalidValue;
+  }
   return 0;
 }
 
@@ -576,15 +714,15 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
   const int64_t rows = (p.num_kv_slots > 0 && p.num_kv_slots < 0x7fffffff) ? p.num_kv_slots : 0x7fffffff;
   thread_local const void* cached_kv = nullptr;
   thread_local int64_t cached_rows = -1;
-  thread_local CUtensorMap tm_tile, tm_gather;
+  thread_local KvMaps maps;
   if (cached_kv != a.kv || cached_rows != rows) {
-    const int rc = make_kv_maps(a.kv, rows, &tm_tile, &tm_gather);
+    const int rc = make_kv_maps(a.kv, rows, &maps);
     if (rc != 0) return rc;
     cached_kv = a.kv;
     cached_rows = rows;
   }
   mla_stage1_fp8_umma_kernel<<<p.num_ctas, kThreadsU, SU::kAlloc, static_cast<cudaStream_t>(stream)>>>(
-      a, p, tm_tile, tm_gather, (int32_t)rows);
+      a, p, maps, (int32_t)rows);
   return (int)cudaGetLastError();
 }
 
