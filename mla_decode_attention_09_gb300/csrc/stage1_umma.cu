@@ -355,10 +355,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         bool ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
         ready = ready && (i < kRopeStages || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
         if (__shfl_sync(~0u, ready, 0)) {
+          // Box loads when the valid rows are consecutive. A tail tile may then
+          // read rows past the item (other rows of the pool, or zeros past its
+          // end): only done when the pool size is known, and the softmax zeroes
+          // those value rows before P.V reads them.
+          const int nv = c.t_end - c.t0;
           const int y0 = __shfl_sync(~0u, y0s[0], 0);
-          bool cont = (c.t_end - c.t0 >= kRowsU) && y0 != oob_row;
+          bool cont = y0 != oob_row && (nv >= kRowsU || p.num_kv_slots > 0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) cont = cont && (y0s[j] == y0 + lane + 32 * j);
+          for (int j = 0; j < 4; ++j) cont = cont && (lane + 32 * j >= nv || y0s[j] == y0 + lane + 32 * j);
           cont = __all_sync(~0u, cont);
           const uint32_t fb = bar(kBFull + ls);
           const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
@@ -586,6 +591,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           l[4 * j + 1] += f01.y;
           l[4 * j + 2] += f23.x;
           l[4 * j + 3] += f23.y;
+        }
+        if (ok && row >= nv) {  // row past the item: its value row may hold anything; P.V must see zeros
+          uint8_t* vrow = smem + SU::kLat + (i % kLatStages) * kLatStage + row * 128;
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(vrow + cb * kBlk + ch * 16) = make_uint4(0, 0, 0, 0);
         }
         if (ok && i >= 2) ok = wait_u(bar(kBPEmpty + (i & 1)), ((i >> 1) - 1) & 1, abort_flag);
         if (ok)
