@@ -82,7 +82,8 @@ typedef struct mla_plan_options {
                              kernel (out-of-range rows are skipped and MLA_ERR_INDEX recorded).
                              0 = unchecked (the plain mla_decode_plan) */
   int min_rows_per_split; /* smallest KV chunk the planner cuts (default 256) */
-  int granularity;        /* chunk boundaries are multiples of this many rows (default 16) */
+  int granularity;        /* work is balanced in units of this many rows, and chunk boundaries fall on
+                             multiples of it from the sequence start (default 128, the fp8 kernel's tile) */
   int ctas_per_sm;        /* persistent CTAs per SM (default 1) */
   int fp8_kernel;         /* fp8 stage-1 kernel: 0 = 5th-generation tensor cores (tcgen05 + TMA, default),
                              1 = warp-level mma.sync (kept for comparison) */

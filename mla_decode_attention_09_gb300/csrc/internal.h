@@ -54,7 +54,7 @@ struct HostPlan {
 struct PlanOptions {
   int64_t num_kv_slots = 0;
   int min_rows_per_split = 256;
-  int granularity = 16;
+  int granularity = 128;  // the tcgen05 kernel's tile height (a multiple of the warp-level kernels' 64)
   int ctas_per_sm = 1;
   int fp8_kernel = 0;  // 0 = tcgen05 / TMA kernel, 1 = warp-level mma.sync kernel
 };

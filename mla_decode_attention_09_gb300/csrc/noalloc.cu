@@ -74,9 +74,9 @@ void setup_device(int dev, DeviceSetup* s) {
   s->status = MLA_OK;
 }
 
-// Work list in fixed-capacity arrays (no heap): the same global-cut split as
-// the regular planner with its default options (16-row granules, chunks of at
-// least 256 rows, one CTA per SM).
+// Work list in fixed-capacity arrays (no heap): the same split as the
+// regular planner with its default options (128-row granules balanced across
+// CTAs, chunks of at least 256 rows, one CTA per SM).
 struct FixedPlan {
   WorkItem items[kMaxItems];
   int32_t indptr[kMaxCtas + 1];
@@ -87,32 +87,33 @@ struct FixedPlan {
 
 // Returns MLA_OK, MLA_ERR_INDPTR, or MLA_ERR_NOALLOC_LIMIT when a fixed capacity is exceeded.
 int plan_fixed(int batch, const int32_t* ip, int num_sms, FixedPlan* fp) {
-  constexpr int64_t G = 16, kMinRows = 256;
+  constexpr int64_t G = 128, kMinRows = 256;
   if (ip[0] != 0) return MLA_ERR_INDPTR;
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) {
     if (ip[b + 1] < ip[b]) return MLA_ERR_INDPTR;
     total += (int64_t)ip[b + 1] - ip[b];
   }
+  // granules of G rows per sequence (no prefix-sum array: the cut loop below
+  // walks the sequences forward once instead)
+  int64_t U = 0;
+  for (int b = 0; b < batch; ++b) U += ((int64_t)ip[b + 1] - ip[b] + G - 1) / G;
   const int64_t max_ctas = std::min<int64_t>(num_sms, kMaxCtas);
-  int64_t target = total > 0 ? (total + max_ctas - 1) / max_ctas : 1;
-  target = std::max<int64_t>(target, kMinRows);
-  target = (target + G - 1) / G * G;
-  const int64_t n = total > 0 ? std::min<int64_t>(max_ctas, (total + target - 1) / target) : 1;
+  int64_t target = U > 0 ? (U + max_ctas - 1) / max_ctas : 1;
+  target = std::max<int64_t>(target, (kMinRows + G - 1) / G);
+  const int64_t n = U > 0 ? std::min<int64_t>(max_ctas, (U + target - 1) / target) : 1;
   fp->cuts[0] = 0;
   fp->cuts[n] = total;
+  int b = 0;
+  int64_t gb = 0;  // granules before sequence b
   for (int64_t k = 1; k < n; ++k) {
-    const int64_t P = total * k / n;
-    int lo = 0, hi = batch - 1;  // sequence holding row P: last b with ip[b] <= P
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) / 2;
-      if ((int64_t)ip[mid] <= P) lo = mid; else hi = mid - 1;
+    const int64_t g = U * k / n;  // increasing in k: the scan over sequences only moves forward
+    while (b < batch - 1 && gb + ((int64_t)ip[b + 1] - ip[b] + G - 1) / G <= g) {
+      gb += ((int64_t)ip[b + 1] - ip[b] + G - 1) / G;
+      ++b;
     }
-    const int64_t S = ip[lo], L = (int64_t)ip[lo + 1] - S;
-    int64_t r = (P - S + G / 2) / G * G;
-    if (r < G) r = 0;
-    if (L - r < G) r = L;
-    fp->cuts[k] = std::max(fp->cuts[k - 1], S + r);
+    const int64_t S = ip[b], L = (int64_t)ip[b + 1] - S;
+    fp->cuts[k] = S + std::min<int64_t>((g - gb) * G, L);
   }
   // keep only non-empty ranges: range c = [cuts[c], cuts[c+1])
   int64_t m = 0;

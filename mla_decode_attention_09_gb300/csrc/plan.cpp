@@ -6,12 +6,12 @@
 // kv_granularity = max(page_size, 16) there). Their field layout belongs to a
 // closed library and is not shown, so this planner defines its own: the rows
 // of all sequences, laid end to end, are cut into one contiguous range per
-// persistent CTA of nearly equal length. A sequence that lies inside one range
-// is a single work item writing its final output; a sequence that straddles
-// cuts becomes several items writing partial (O, LSE) slots that the reduce
-// merges. Cuts fall on multiples of `granularity` rows from the sequence
-// start, and no range is shorter than `min_rows_per_split` unless the whole
-// problem is.
+// persistent CTA holding the same number of `granularity`-row granules (to
+// within one). A sequence that lies inside one range is a single work item
+// writing its final output; a sequence that straddles cuts becomes several
+// items writing partial (O, LSE) slots that the reduce merges. Cuts fall on
+// multiples of `granularity` rows from the sequence start, and no range is
+// shorter than `min_rows_per_split` unless the whole problem is.
 #include <algorithm>
 #include <utility>
 #include <cstdlib>
@@ -55,32 +55,34 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
   }
   out->total_rows = total;
 
+  // Work is counted in granules: sequence b is ceil(L_b / G) granules of G
+  // rows (its last one may be shorter). The granules of all sequences, laid
+  // end to end, are divided evenly among the ranges, so every range gets the
+  // same number of granules to within one and every cut falls on a multiple of
+  // G rows from its sequence's start. With G equal to the kernels' tile height
+  // the ranges hold the same number of tiles to within one.
   const int64_t G = opt.granularity;
   const int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
-  int64_t target = total > 0 ? (total + max_ctas - 1) / max_ctas : 1;
-  target = std::max<int64_t>(target, opt.min_rows_per_split);
-  target = (target + G - 1) / G * G;
-  const int64_t n_ranges = total > 0 ? std::min<int64_t>(max_ctas, (total + target - 1) / target) : 1;
+  std::vector<int64_t> gstart((size_t)batch + 1, 0);
+  for (int b = 0; b < batch; ++b)
+    gstart[(size_t)b + 1] = gstart[(size_t)b] + ((int64_t)kv_indptr[b + 1] - kv_indptr[b] + G - 1) / G;
+  const int64_t U = gstart[(size_t)batch];
+  int64_t target = U > 0 ? (U + max_ctas - 1) / max_ctas : 1;
+  target = std::max<int64_t>(target, (opt.min_rows_per_split + G - 1) / G);
+  const int64_t n_ranges = U > 0 ? std::min<int64_t>(max_ctas, (U + target - 1) / target) : 1;
 
-  // Global cut points: the ideal cut k * total / n, moved to the nearest
-  // multiple of G from the start of the sequence it falls in (or to that
-  // sequence's start / end when less than G rows would be left on a side).
-  // Cuts are absolute, so snapping errors never accumulate.
   std::vector<int64_t> cuts((size_t)n_ranges + 1, 0);
   cuts[(size_t)n_ranges] = total;
   for (int64_t k = 1; k < n_ranges; ++k) {
-    const int64_t P = total * k / n_ranges;
-    // sequence containing row P: last b with kv_indptr[b] <= P (it is non-empty since P < total)
+    const int64_t g = U * k / n_ranges;
+    // sequence holding granule g: last b with gstart[b] <= g (it has granules since g < U)
     int lo = 0, hi = batch - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) / 2;
-      if ((int64_t)kv_indptr[mid] <= P) lo = mid; else hi = mid - 1;
+      if (gstart[(size_t)mid] <= g) lo = mid; else hi = mid - 1;
     }
     const int64_t S = kv_indptr[lo], L = (int64_t)kv_indptr[lo + 1] - S;
-    int64_t r = (P - S + G / 2) / G * G;
-    if (r < G) r = 0;
-    if (L - r < G) r = L;
-    cuts[(size_t)k] = std::max(cuts[(size_t)k - 1], S + r);
+    cuts[(size_t)k] = S + std::min<int64_t>((g - gstart[(size_t)lo]) * G, L);
   }
   std::vector<std::pair<int64_t, int64_t>> ranges;  // non-empty CTA row ranges, in order
   for (int64_t k = 0; k < n_ranges; ++k)

@@ -68,7 +68,7 @@ MODE_IDS = ["bf16", "fp8-tcgen05", "fp8-mma"]
 @pytest.mark.parametrize("split", ["whole", "split"])
 def test_odd_lengths(mla, mode, k8, split):
     inp = mi.make_inputs(ODD, mode, seed=100 + mode, permute=True, extra_slots=37)
-    opts = {} if split == "whole" else {"min_rows_per_split": 16}
+    opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
     out, plan = run(mla, inp, num_sms=152 if split == "whole" else 5, fp8_kernel=k8, **opts)
     info = plan.info()
     if split == "split":
@@ -79,7 +79,7 @@ def test_odd_lengths(mla, mode, k8, split):
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_one_long_sequence_many_splits(mla, mode, k8):
     inp = mi.make_inputs([5003], mode, seed=7)
-    out, plan = run(mla, inp, num_sms=152, min_rows_per_split=16, fp8_kernel=k8)
+    out, plan = run(mla, inp, num_sms=152, min_rows_per_split=16, granularity=16, fp8_kernel=k8)
     assert plan.info()["num_partial_slots"] > 100
     compare(out, oracle_out(inp), mode, "one long sequence")
 

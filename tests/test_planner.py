@@ -10,7 +10,7 @@ def _check_plan(lengths, num_sms, **opts):
     ip[1:] = np.cumsum(lengths)
     r = mla.plan_compute_host(ip, num_sms, **opts)
     items, wip, red = r["items"], r["work_indptr"], r["reduce"]
-    G = opts.get("granularity", 16)
+    G = opts.get("granularity", 128)
     min_split = opts.get("min_rows_per_split", 256)
     cpsm = opts.get("ctas_per_sm", 1)
     total = int(ip[-1])
@@ -43,14 +43,18 @@ def _check_plan(lengths, num_sms, **opts):
             next_slot += n
             assert all(t1 > t0 for t0, t1, _ in parts), "no empty partial"
     assert next_slot == r["num_slots"]
-    # load balance: no CTA above the target (rounded to G) plus two granules
+    # load balance in granules (G rows; a sequence's last granule may be shorter): every CTA
+    # holds floor or ceil of (granules / CTAs), and no CTA more than the target
     if total:
         max_ctas = num_sms * cpsm
-        target = max(-(-total // max_ctas), min_split)
-        target = -(-target // G) * G
+        U = sum(-(-L // G) for L in lengths)
+        target = max(-(-U // max_ctas), -(-min_split // G))
+        gran = [sum(-(-int(items[i, 2] - items[i, 1]) // G) for i in range(wip[c], wip[c + 1]))
+                for c in range(r["num_ctas"])]
+        assert sum(gran) == U
+        assert max(gran) <= target
+        assert max(gran) - min(gran) <= 1
         rows = [sum(int(items[i, 2] - items[i, 1]) for i in range(wip[c], wip[c + 1])) for c in range(r["num_ctas"])]
-        # each cut moves less than G from its ideal position
-        assert max(rows) <= target + 2 * G
         assert sum(rows) == total
     return r
 
@@ -75,7 +79,7 @@ def test_plan_invariants_random():
         if rng.random() < 0.5:
             opts["min_rows_per_split"] = int(rng.choice([16, 64, 256, 1024]))
         if rng.random() < 0.3:
-            opts["granularity"] = int(rng.choice([1, 8, 16, 64]))
+            opts["granularity"] = int(rng.choice([1, 8, 16, 64, 128]))
         _check_plan(lengths, int(rng.integers(1, 160)), **opts)
 
 
@@ -87,6 +91,11 @@ def test_plan_headline_shapes():
     # B=4 x 1024 bf16: small problem, minimum chunk keeps the split count low
     r = _check_plan([1024] * 4, 152)
     assert r["num_ctas"] == 16
+    # every CTA gets 26 or 27 of the 4096 tiles of B=64 x 8192
+    r = mla.plan_compute_host(np.arange(65, dtype=np.int32) * 8192, 152)
+    tiles = [sum(-(-int(t1 - t0) // 128) for _, t0, t1, _, _ in r["items"][r["work_indptr"][c]:r["work_indptr"][c + 1]])
+             for c in range(152)]
+    assert set(tiles) <= {26, 27}
 
 
 def test_plan_rejects_bad_indptr():
