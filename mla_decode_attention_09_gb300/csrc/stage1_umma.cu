@@ -531,35 +531,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
 #pragma unroll
         for (int h = 0; h < 16; ++h) x[h] = (ok && row < nv) ? x[h] * score_log2 : -INFINITY;
-        const float mh = xreduce16<true>(x, lane);
-        float* rb = red + (i & 1) * 64;
-        if (!(lane & 1)) rb[(lane >> 1) * 4 + warp] = mh;
-        if (ptx::named_bar_or(1, 128, !ok)) {
-          aborted = true;
-          break;
-        }
-        float tmax[16];
+        // Fast path: every score within 2^tau of the reference max needs no
+        // tile max (one barrier ORs the check). A timed-out wait also takes the
+        // full path, whose barrier then stops every thread.
+        const bool first = t0 == w.t_begin;
+        bool local_need = first || !ok;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float4 v = *reinterpret_cast<const float4*>(rb + 4 * h);
-          tmax[h] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-        }
-        if (t0 == w.t_begin) {
+        for (int h = 0; h < 16; ++h) local_need |= x[h] > m_ref[h] + kTau;
+        if (ptx::named_bar_or(1, 128, local_need)) {
+          const float mh = xreduce16<true>(x, lane);
+          float* rb = red + (i & 1) * 64;
+          if (!(lane & 1)) rb[(lane >> 1) * 4 + warp] = mh;
+          if (ptx::named_bar_or(1, 128, !ok)) {
+            aborted = true;
+            break;
+          }
+          float tmax[16], alpha[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) m_ref[h] = tmax[h];
-        } else {
-          bool need = false;
-#pragma unroll
-          for (int h = 0; h < 16; ++h) need |= tmax[h] > m_ref[h] + kTau;
-          if (need) {  // rare: move the reference up and rescale O (after P.V of the previous tile lands)
-            float alpha[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) {
-              const float mn = fmaxf(m_ref[h], tmax[h]);
-              alpha[h] = ptx::ex2(m_ref[h] - mn);
-              m_ref[h] = mn;
-              l[h] *= alpha[h];
-            }
+          for (int h = 0; h < 16; ++h) {
+            const float4 v = *reinterpret_cast<const float4*>(rb + 4 * h);
+            tmax[h] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+            const float mn = fmaxf(m_ref[h], tmax[h]);
+            alpha[h] = ptx::ex2(m_ref[h] - mn);
+            m_ref[h] = mn;
+            l[h] *= alpha[h];
+          }
+          if (!first) {  // move the reference up: rescale O once P.V of the previous tile has landed
             const int pt = i - 1;
             if (__all_sync(~0u, wait_u(bar(kBPEmpty + (pt & 1)), (pt >> 1) & 1, abort_flag))) {
               umma::fence_after_sync();
