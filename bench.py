@@ -164,24 +164,31 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def stage1_source_sha() -> str:
+STAGE1_KERNELS = {
+    # kernel name -> (profile file stem, sources whose bytes identify the compiled kernel)
+    "mla_stage1_fp8_umma_kernel": ("stage1_umma", ("stage1_umma.cu", "umma.cuh", "ptx.cuh", "internal.h")),
+    "mla_stage1_kernel": ("stage1_mma", ("stage1.cu", "ptx.cuh", "internal.h")),
+}
+
+
+def stage1_source_sha(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_09_gb300", "csrc")
-    for f in ("stage1.cu", "ptx.cuh", "internal.h"):
+    for f in STAGE1_KERNELS[kernel][1]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per stage-1 launch from the committed ncu summary, if it matches the current kernel source."""
-    path = os.path.join(PROFILES, f"stage1_{workload}.json")
+    path = os.path.join(PROFILES, f"{STAGE1_KERNELS[kernel][0]}_{workload}.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_sha") != stage1_source_sha():
+    if d.get("source_sha") != stage1_source_sha(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -297,10 +304,11 @@ def bench_ours(args):
     stage1_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     peak, peak_kind = measured_peak()
     achieved = step_bytes / (stage1_ms * 1e-3) / 1e9
+    kernel = ("mla_stage1_fp8_umma_kernel" if (w.mode == mi.MODE_FP8 and args.fp8_kernel == 0)
+              else "mla_stage1_kernel")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
-                "kernel": ("mla_stage1_fp8_umma_kernel" if (w.mode == mi.MODE_FP8 and args.fp8_kernel == 0)
-                           else "mla_stage1_kernel"), "peak_kind": peak_kind,
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kernel, args.workload),
+                "kernel": kernel, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": step_bytes, "stage1_us": round(stage1_ms * 1e3, 2)}
 
     e2e = None
