@@ -61,6 +61,16 @@ def barrier(ws):
         torch.distributed.barrier()
 
 
+def replica_seed_offset(rank: int, copy: int) -> int:
+    """Seed offset of input copy `copy` on `rank`: every rank holds its own independent replica."""
+    return 1000 * rank + copy
+
+
+def whole_job_gbs(step_bytes: int, steps: int, ws: int, ms_max: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed over the slowest rank's time."""
+    return step_bytes * steps * ws / (ms_max * 1e-3) / 1e9
+
+
 def max_over_ranks(x: float, ws: int, device) -> float:
     if ws == 1:
         return x
@@ -223,7 +233,7 @@ def bench_ours(args):
     step_bytes = nbytes["total"]
 
     # two input copies, each larger than L2 for the headline workload (seeded per rank: independent replicas)
-    devs = [mi.make_workload(w, device=str(dev), seed_offset=1000 * rank + k) for k in range(2)]
+    devs = [mi.make_workload(w, device=str(dev), seed_offset=replica_seed_offset(rank, k)) for k in range(2)]
     scales = [d.kv_scale_tensor(dev) for d in devs]
     plan = mla.plan(devs[0].kv_indptr.cpu(), 0, num_kv_slots=devs[0].kv.shape[0], fp8_kernel=args.fp8_kernel)
     info = plan.info()
@@ -285,7 +295,7 @@ def bench_ours(args):
     if status != 0:
         raise RuntimeError(f"kernel error status {status}")
     ms_per_step = ms_max / args.steps
-    value = step_bytes * args.steps * ws / (ms_max * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, args.steps, ws, ms_max)
     launches_per_step = 1 + (1 if info["num_split_seqs"] > 0 else 0)
 
     # roofline of the dominant kernel: stage 1 alone, each launch bracketed by events on its stream
