@@ -287,20 +287,24 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     }
     const uint64_t pol = ptx::l2_evict_first_policy();
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    // row sources of one tile held by this lane: rows lane + 32 j (index loads run two tiles ahead)
+    // row sources of one tile held by this lane: rows lane + 32 j. Index loads run two tiles
+    // ahead and are checked only when the tile is issued, so the loads stay in flight meanwhile.
     auto load_rows = [&](const TCur& t, int (&y)[4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = lane + 32 * j;
-        int v = oob_row;
-        if (!t.done && r < t.t_end - t.t0) {
-          const int idx = __ldg(a.kv_indices + t.base + t.t0 + r);
-          if (idx >= 0 && (p.num_kv_slots == 0 || idx < p.num_kv_slots))
-            v = idx;
-          else
-            record_error_u(p.err, MLA_ERR_INDEX);
+        y[j] = (!t.done && r < t.t_end - t.t0) ? __ldg(a.kv_indices + t.base + t.t0 + r) : oob_row;
+      }
+    };
+    auto check_rows = [&](int nv, int (&y)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (lane + 32 * j >= nv) {
+          y[j] = oob_row;
+        } else if (y[j] < 0 || (p.num_kv_slots > 0 && y[j] >= p.num_kv_slots)) {
+          record_error_u(p.err, MLA_ERR_INDEX);
+          y[j] = oob_row;
         }
-        y[j] = v;
       }
     };
     // query of one item as e4m3, 8 bytes per chunk of 8 dims; lane holds chunks lane + 32 j
@@ -324,7 +328,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       umma::mbar_arrive(bar(kBQFull));
     };
 
-    TCur c, c1, c2, qc;  // c: next tile to load; c1, c2: the two after; qc: item whose query is next
+    // c: next tile to load; c1, c2: the two after. qc: item whose query is staged next.
+    // Tile loads come first. Loading and casting a query stalls the warp on global
+    // loads, so it runs only when no tile can be issued (the ring is full, or every
+    // tile is issued); the first item's query lands while its first tiles are in flight.
+    TCur c, c1, c2, qc;
     tcur_init(c, item_begin, item_end, p, a.kv_indptr);
     c1 = c;
     tcur_next(c1, p, a.kv_indptr);
@@ -334,32 +342,24 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     int y0s[4], y1s[4];
     load_rows(c, y0s);
     load_rows(c1, y1s);
-    if (!qc.done) load_q(qc.b);
+    bool q_loaded = false, q_advance = false;
     int i = 0;
     bool ok = true;
     IdleClock idle;
     while (!c.done || !qc.done) {
-      bool progress = false;
-      // query of item qc.k: the single buffer frees when the last scores of item qc.k - 1 complete
-      if (!qc.done) {
-        const bool free_ = qc.k == 0 || ptx::mbar_test_wait(bar(kBQEmpty), (qc.k - 1) & 1);
-        if (__shfl_sync(~0u, free_, 0)) {
-          store_q();
-          tcur_next_item(qc, p, a.kv_indptr);
-          if (!qc.done) load_q(qc.b);
-          progress = true;
-        }
-      }
+      bool progress = false, tile_blocked = c.done;
       if (!c.done) {
         const int ls = i % kLatStages, rs = i & 1;
         bool ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
         ready = ready && (i < kRopeStages || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
-        if (__shfl_sync(~0u, ready, 0)) {
+        tile_blocked = !__shfl_sync(~0u, ready, 0);
+        if (!tile_blocked) {
           // Box loads when the valid rows are consecutive. A tail tile may then
           // read rows past the item (other rows of the pool, or zeros past its
           // end): only done when the pool size is known, and the softmax zeroes
           // those value rows before P.V reads them.
           const int nv = c.t_end - c.t0;
+          check_rows(nv, y0s);
           const int y0 = __shfl_sync(~0u, y0s[0], 0);
           bool cont = y0 != oob_row && (nv >= kRowsU || p.num_kv_slots > 0);
 #pragma unroll
@@ -398,6 +398,30 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           tcur_next(c2, p, a.kv_indptr);
           ++i;
           progress = true;
+        }
+      }
+      // query of item qc.k: the single buffer frees when the last scores of item qc.k - 1 complete
+      if (!qc.done) {
+        if (!q_loaded) {
+          if (tile_blocked) {
+            if (q_advance) {
+              tcur_next_item(qc, p, a.kv_indptr);
+              q_advance = false;
+            }
+            if (!qc.done) {
+              load_q(qc.b);
+              q_loaded = true;
+            }
+            progress = true;
+          }
+        } else {
+          const bool free_ = qc.k == 0 || ptx::mbar_test_wait(bar(kBQEmpty), (qc.k - 1) & 1);
+          if (__shfl_sync(~0u, free_, 0)) {
+            store_q();
+            q_loaded = false;
+            q_advance = true;
+            progress = true;
+          }
         }
       }
       if (progress) {
