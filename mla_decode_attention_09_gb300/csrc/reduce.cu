@@ -6,7 +6,10 @@
 // out = sum_s 2^{lse_s - L} O_s, rounded to bf16.
 //
 // One CTA of 128 threads per (split sequence, head); each thread owns 4 of the
-// 512 output dims, so every partial row is read once with 16-byte loads.
+// 512 output dims, so every partial row is read once with 16-byte loads. Every
+// warp finds the max and the sum of 2^(lse - max) with one slot per lane, and
+// the partial rows are read eight slots at a time so that several loads are in
+// flight per thread.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -19,29 +22,55 @@ namespace mla {
 namespace {
 
 constexpr int kReduceThreads = kVDim / 4;  // 128
+constexpr int kUnroll = 8;
+
+__device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
+  acc.x = fmaf(w, v.x, acc.x);
+  acc.y = fmaf(w, v.y, acc.y);
+  acc.z = fmaf(w, v.z, acc.z);
+  acc.w = fmaf(w, v.w, acc.w);
+}
 
 __global__ void __launch_bounds__(kReduceThreads)
     mla_reduce_kernel(const DevicePlan p, __nv_bfloat16* __restrict__ out, int use_pdl) {
   if (use_pdl) ptx::griddep_wait();  // stage 1 of this decode has finished writing the partials
+  // the next kernel in the stream may start its prologue; it waits for this grid before touching memory
+  ptx::griddep_launch_dependents();
   const int e = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
   if (e >= p.n_reduce) return;
+  const int lane = threadIdx.x & 31;
   const ReduceEntry r = p.reduce[e];
+  const int n = r.n_slots;
   const float* lse = p.part_lse + (int64_t)r.slot_begin * kHeads + h;
   float m = -INFINITY;
-  for (int s = 0; s < r.n_slots; ++s) m = fmaxf(m, lse[(int64_t)s * kHeads]);
+  for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[(int64_t)s * kHeads]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (m != -INFINITY) {
     float z = 0.f;
-    for (int s = 0; s < r.n_slots; ++s) z += exp2f(lse[(int64_t)s * kHeads] - m);
+    for (int s = lane; s < n; s += 32) z += exp2f(lse[(int64_t)s * kHeads] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(~0u, z, o);
     const float inv_z = 1.0f / z;
     const float* po = p.part_o + ((int64_t)r.slot_begin * kHeads + h) * kVDim + 4 * threadIdx.x;
-    for (int s = 0; s < r.n_slots; ++s) {
-      const float wgt = exp2f(lse[(int64_t)s * kHeads] - m) * inv_z;
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(po + (int64_t)s * kHeads * kVDim));
-      acc.x += wgt * v.x;
-      acc.y += wgt * v.y;
-      acc.z += wgt * v.z;
-      acc.w += wgt * v.w;
+    constexpr int64_t kSlotStride = (int64_t)kHeads * kVDim;
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      // lane j holds the weight of slot s0 + j
+      const int cnt = min(32, n - s0);
+      const float wl = lane < cnt ? exp2f(lse[(int64_t)(s0 + lane) * kHeads] - m) * inv_z : 0.f;
+      int j = 0;
+      for (; j + kUnroll <= cnt; j += kUnroll) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(po + (s0 + j + u) * kSlotStride));
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) fma4(acc, __shfl_sync(~0u, wl, j + u), v[u]);
+      }
+      for (; j < cnt; ++j) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(po + (s0 + j) * kSlotStride));
+        fma4(acc, __shfl_sync(~0u, wl, j), v);
+      }
     }
   }
   uint2 packed;

@@ -192,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   if ((int)blockIdx.x >= p.num_ctas) return;
-  const int item_begin = p.work_indptr[blockIdx.x], item_end = p.work_indptr[blockIdx.x + 1];
 
   const uint32_t ring = ptx::smem_addr(smem);
   uint8_t* pbuf = smem + S::kPOff;
@@ -205,6 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   ptx::griddep_launch_dependents();
+  // The launch allows this grid to start while the previous kernel in the
+  // stream finishes; wait for that kernel's completion before any global access.
+  ptx::griddep_wait();
+  const int item_begin = p.work_indptr[blockIdx.x], item_end = p.work_indptr[blockIdx.x + 1];
 
   // Tiles this CTA will process (same skipping rules as the item loop below).
   int n_tiles = 0;
@@ -519,8 +522,18 @@ int launch_stage1_t(const DecodeArgs& a, const DevicePlan& p, const uint8_t* zer
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   if (p.num_ctas <= 0) return 0;
-  mla_stage1_kernel<MODE><<<p.num_ctas, kThreads, smem_bytes, stream>>>(a, p, zero_row);
-  return (int)cudaGetLastError();
+  // programmatic stream serialisation: the prologue may overlap the previous kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_kernel<MODE>, a, p, zero_row);
 }
 
 }  // namespace

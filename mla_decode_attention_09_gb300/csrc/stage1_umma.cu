@@ -233,7 +233,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((int)blockIdx.x >= p.num_ctas) return;
-  const int item_begin = p.work_indptr[blockIdx.x], item_end = p.work_indptr[blockIdx.x + 1];
 
   // 1024-aligned base for the swizzle atoms
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -273,6 +272,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SU::kTmemSlot);
   ptx::griddep_launch_dependents();
+  // The launch allows this grid to start while the previous kernel in the
+  // stream finishes: everything above touches only this CTA's shared memory and
+  // TMEM. Wait for that kernel's completion before any global memory access.
+  ptx::griddep_wait();
+  const int item_begin = p.work_indptr[blockIdx.x], item_end = p.work_indptr[blockIdx.x + 1];
 
   const float kv_scale = __ldg(a.kv_scale);
   const float score_log2 = a.sm_scale * kv_scale * kLog2eU;
@@ -754,9 +758,17 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
     cached_kv = a.kv;
     cached_rows = rows;
   }
-  mla_stage1_fp8_umma_kernel<<<p.num_ctas, kThreadsU, SU::kAlloc, static_cast<cudaStream_t>(stream)>>>(
-      a, p, maps, (int32_t)rows);
-  return (int)cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.num_ctas);
+  cfg.blockDim = dim3(kThreadsU);
+  cfg.dynamicSmemBytes = SU::kAlloc;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel, a, p, maps, (int32_t)rows);
 }
 
 }  // namespace mla
