@@ -8,8 +8,11 @@ distributions: Q and KV ~ N(0,1) rounded to bf16 (the pages argue from Q
 being randn with std ~1 — kernelbot amd-mixed-mla submission 689529
 "MLA decode V3", docstring); fp8 KV is the bf16 KV quantised per tensor to
 OCP e4m3fn with kv_scale = amax|KV| / 448 (the pages receive kv_data["fp8"]
-as (buffer, scale) but do not show how it was made); page_size = 1, so
-kv_indptr / kv_indices address single rows.
+as (buffer, scale) but do not show how it was made). The benchmark workloads
+use page_size = 1, so kv_indptr / kv_indices address single rows; paged inputs
+(make_paged_inputs) view the buffer as [num_pages, page_size, 576] with
+kv_indptr counting pages, kv_indices holding page ids and kv_last_page_len the
+tokens used in each sequence's last page (submission 641982 "v86", _run_a8w8).
 """
 from __future__ import annotations
 
@@ -64,9 +67,11 @@ class Inputs:
     q: torch.Tensor            # bf16 [B,16,576]
     kv: torch.Tensor           # bf16 [slots,576] (mode 0) or uint8 e4m3 codes [slots,576]
     kv_scale: float            # per-tensor fp32 dequantisation scale (1.0 in mode 0)
-    kv_indptr: torch.Tensor    # int32 [B+1]
-    kv_indices: torch.Tensor   # int32 [R]
+    kv_indptr: torch.Tensor    # int32 [B+1] (pages when page_size > 1)
+    kv_indices: torch.Tensor   # int32 [R] (page ids when page_size > 1)
     sm_scale: float = SM_SCALE
+    page_size: int = 1
+    kv_last_page_len: torch.Tensor | None = None   # int32 [B] when page_size > 1
 
     @property
     def batch(self) -> int:
@@ -74,7 +79,8 @@ class Inputs:
 
     @property
     def rows(self) -> int:
-        return int(self.kv_indptr[-1])
+        """KV rows (tokens) the decode reads."""
+        return int(self.lengths().sum())
 
     @property
     def kv_row_bytes(self) -> int:
@@ -84,12 +90,19 @@ class Inputs:
         return torch.tensor([self.kv_scale], dtype=torch.float32, device=device)
 
     def to(self, device) -> "Inputs":
+        lp = None if self.kv_last_page_len is None else self.kv_last_page_len.to(device)
         return Inputs(self.mode, self.q.to(device), self.kv.to(device), self.kv_scale,
-                      self.kv_indptr.to(device), self.kv_indices.to(device), self.sm_scale)
+                      self.kv_indptr.to(device), self.kv_indices.to(device), self.sm_scale, self.page_size, lp)
 
     def lengths(self) -> np.ndarray:
+        """Tokens per sequence."""
         ip = self.kv_indptr.cpu().numpy().astype(np.int64)
-        return ip[1:] - ip[:-1]
+        pages = ip[1:] - ip[:-1]
+        if self.page_size == 1 and self.kv_last_page_len is None:
+            return pages
+        last = (np.full(pages.shape, self.page_size, np.int64) if self.kv_last_page_len is None
+                else self.kv_last_page_len.cpu().numpy().astype(np.int64))
+        return np.where(pages > 0, (pages - 1) * self.page_size + last, 0)
 
 
 def quantize_kv_e4m3(kv_bf16: torch.Tensor) -> tuple[torch.Tensor, float]:
@@ -127,6 +140,39 @@ def make_inputs(lengths, mode: int, seed: int, permute: bool = False, extra_slot
         return Inputs(mode, q, kv.contiguous(), 1.0, kv_indptr, kv_indices)
     codes, scale = quantize_kv_e4m3(kv)
     return Inputs(mode, q, codes.contiguous(), scale, kv_indptr, kv_indices)
+
+
+def make_paged_inputs(lengths, page_size: int, mode: int, seed: int, permute: bool = False, extra_pages: int = 0,
+                      q_std: float = 1.0, device: str = "cpu") -> Inputs:
+    """Seeded inputs in the paged layout: sequence b takes ceil(L_b / page_size)
+    pages, the last one holding L_b - (pages - 1) * page_size tokens (its other
+    rows are unused and hold random data). Pages are taken in order unless
+    ``permute`` shuffles the page order; ``extra_pages`` adds unused pages."""
+    lengths = [int(x) for x in lengths]
+    ps = int(page_size)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    batch = len(lengths)
+    pages = [(L + ps - 1) // ps for L in lengths]
+    last = [L - (p - 1) * ps if p > 0 else 1 for L, p in zip(lengths, pages)]
+    total_pages = sum(pages)
+    pool_pages = total_pages + int(extra_pages)
+    rows = pool_pages * ps
+    q = (torch.randn((batch, HEADS, QK_DIM), generator=g, device=device) * q_std).to(torch.bfloat16)
+    kv = torch.randn((max(rows, 1), QK_DIM), generator=g, device=device).to(torch.bfloat16)[:rows]
+    ip = torch.zeros(batch + 1, dtype=torch.int64)
+    if batch:
+        ip[1:] = torch.cumsum(torch.tensor(pages, dtype=torch.int64), 0)
+    kv_indptr = ip.to(torch.int32).to(device)
+    if permute:
+        kv_indices = torch.randperm(pool_pages, generator=g, device=device)[:total_pages].to(torch.int32)
+    else:
+        kv_indices = torch.arange(total_pages, dtype=torch.int32, device=device)
+    lp = torch.tensor(last, dtype=torch.int32, device=device)
+    if mode == MODE_BF16:
+        return Inputs(mode, q, kv.contiguous(), 1.0, kv_indptr, kv_indices, SM_SCALE, ps, lp)
+    codes, scale = quantize_kv_e4m3(kv)
+    return Inputs(mode, q, codes.contiguous(), scale, kv_indptr, kv_indices, SM_SCALE, ps, lp)
 
 
 def workload_lengths(w: Workload) -> list[int]:

@@ -63,6 +63,8 @@ def _declare(lib):
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_decode.argtypes = [i32, P, P, i64, i32, f32, P, P, f64, P, i32, P, P]
     lib.oracle_decode.restype = i32
+    lib.oracle_decode_paged.argtypes = [i32, P, P, i64, i32, f32, P, P, P, i32, f64, P, i32, P, P]
+    lib.oracle_decode_paged.restype = i32
     lib.oracle_decode_range.argtypes = [i32, P, P, i64, i32, f32, P, P, f64, i32, i64, i64, P, P]
     lib.oracle_decode_range.restype = i32
     lib.oracle_combine.argtypes = [i32, P, P, P, P]
@@ -125,6 +127,35 @@ def decode(q, kv, kv_indptr, kv_indices, sm_scale: float, mode: int = 0, kv_scal
                            None if sids is None else _ptr(sids), n, _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_decode failed with code {rc}")
+    return out, lse
+
+
+def decode_paged(q, kv, kv_indptr, kv_indices, kv_last_page_len, page_size: int, sm_scale: float, mode: int = 0,
+                 kv_scale: float = 1.0, seq_ids=None, lib=None):
+    """Oracle MLA decode over a paged KV buffer. Returns (out [n,16,512], lse [n,16]) float64.
+
+    kv: [num_pages * page_size, 576] (the buffer viewed as pages of page_size rows);
+    kv_indptr int32 [B+1] in pages; kv_indices int32 page ids; kv_last_page_len
+    int32 [B] (None: every last page full).
+    """
+    lib = lib or load()
+    qb = _u16(q).reshape(-1)
+    kvb = _kv_bytes(kv, mode)
+    ip = _i32(kv_indptr)
+    ix = _i32(kv_indices)
+    lp = None if kv_last_page_len is None else _i32(kv_last_page_len)
+    batch = ip.shape[0] - 1
+    sids = None if seq_ids is None else _i32(seq_ids)
+    n = batch if sids is None else sids.shape[0]
+    out = np.zeros((n, HEADS, V_DIM), dtype=np.float64)
+    lse = np.zeros((n, HEADS), dtype=np.float64)
+    rc = lib.oracle_decode_paged(batch, _ptr(qb), _ptr(kvb), kvb.size // QK_DIM, mode, float(kv_scale), _ptr(ip),
+                                 _ptr(ix if ix.size else np.zeros(1, np.int32)),
+                                 None if lp is None else _ptr(lp if lp.size else np.zeros(1, np.int32)),
+                                 int(page_size), float(sm_scale), None if sids is None else _ptr(sids), n,
+                                 _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_paged failed with code {rc}")
     return out, lse
 
 

@@ -1,6 +1,6 @@
 /*
  * MLA decode oracle: plain, slow, float64 CPU reference for single-token
- * Multi-head Latent Attention decode over a page_size=1 latent KV cache.
+ * Multi-head Latent Attention decode over a paged latent KV cache.
  *
  * TEST INFRASTRUCTURE ONLY. Nothing on the product path may load or call
  * this library; only the tests, the smoke check and the benchmark's CPU
@@ -18,6 +18,12 @@
  *   O[b,h,j] = sum_t softmax(s)_t * kv[row_t, j] for j < 512, i.e. the value
  *   vectors are the first 512 entries of the very rows used as keys
  *   (V3 passes the single kv buffer once; V6c views it as [pages,1,1,576]).
+ *   Paged addressing (submission 641982 "v86", _run_a8w8, and 598454 "v12",
+ *   custom_kernel): the KV buffer is viewed as [num_pages, page_size, 1, 576],
+ *   kv_indptr counts pages, kv_indices holds page ids and kv_last_page_lens[b]
+ *   is the number of tokens used in sequence b's last page. Token t is entry
+ *   t % page_size of page kv_indices[kv_indptr[b] + t / page_size]; page_size
+ *   1 with every last page full is the row addressing above.
  *   There is no mask: with one query token per sequence it sees all of its KV
  *   (the pages set is_causal both ways; with q_seq_len = 1 the two agree).
  *   logit_cap = 0 on the pages means no cap.
@@ -115,14 +121,34 @@ static double kv_value(const void* kv, int64_t row, int d, int mode, double kv_s
   return oracle_e4m3_decode(((const uint8_t*)kv)[row * ORACLE_QK_DIM + d]) * kv_scale;
 }
 
+/* KV row of token t of a sequence whose page list starts at kv_indices[page_base]. */
+static int64_t token_row(const int32_t* kv_indices, int64_t page_base, int64_t t, int page_size) {
+  return (int64_t)kv_indices[page_base + t / page_size] * page_size + t % page_size;
+}
+
 /*
- * Attention of one head of sequence b over the rows t in [t_begin, t_end) of
- * that sequence. Writes out[0..511] and *lse (natural log of sum_t e^{s_t}).
- * Returns 0, or -1 if a row index is outside [0, num_slots).
+ * Tokens of sequence b: (pages - 1) * page_size + its last page length, or 0
+ * when it has no pages. With no last_page_len array every last page is full.
+ * Returns -1 for a negative page count or a last page length outside
+ * [1, page_size].
+ */
+static int64_t seq_tokens(const int32_t* kv_indptr, const int32_t* last_page_len, int page_size, int b) {
+  int64_t pages = (int64_t)kv_indptr[b + 1] - kv_indptr[b], last;
+  if (pages == 0) return 0;
+  if (pages < 0) return -1;
+  last = last_page_len ? (int64_t)last_page_len[b] : (int64_t)page_size;
+  if (last < 1 || last > page_size) return -1;
+  return (pages - 1) * page_size + last;
+}
+
+/*
+ * Attention of one head of sequence b over its tokens t in [t_begin, t_end).
+ * Writes out[0..511] and *lse (natural log of sum_t e^{s_t}).
+ * Returns 0, or -1 if a token's row is outside [0, num_slots).
  */
 static int attend_head(const uint16_t* q, const void* kv, int64_t num_slots, int mode, double kv_scale,
-                       const int32_t* kv_indptr, const int32_t* kv_indices, double sm_scale, int b, int h,
-                       int64_t t_begin, int64_t t_end, double* out, double* lse) {
+                       const int32_t* kv_indptr, const int32_t* kv_indices, int page_size, double sm_scale, int b,
+                       int h, int64_t t_begin, int64_t t_end, double* out, double* lse) {
   int64_t n = t_end - t_begin, t;
   int d, j;
   double m, z, *s;
@@ -138,7 +164,7 @@ static int attend_head(const uint16_t* q, const void* kv, int64_t num_slots, int
   if (!s) return -2;
   /* scores */
   for (t = 0; t < n; ++t) {
-    int64_t row = kv_indices[base + t_begin + t];
+    int64_t row = token_row(kv_indices, base, t_begin + t, page_size);
     double acc = 0.0;
     if (row < 0 || row >= num_slots) {
       free(s);
@@ -158,7 +184,7 @@ static int attend_head(const uint16_t* q, const void* kv, int64_t num_slots, int
   }
   /* weighted sum of the value vectors = first 512 entries of the same rows */
   for (t = 0; t < n; ++t) {
-    int64_t row = kv_indices[base + t_begin + t];
+    int64_t row = token_row(kv_indices, base, t_begin + t, page_size);
     double w = s[t] / z;
     for (j = 0; j < ORACLE_V_DIM; ++j) out[j] += w * kv_value(kv, row, j, mode, kv_scale);
   }
@@ -168,32 +194,43 @@ static int attend_head(const uint16_t* q, const void* kv, int64_t num_slots, int
 }
 
 /*
- * Full decode for the sequences listed in seq_ids (all B sequences, in order,
- * when seq_ids is NULL). out: [n_seq, 16, 512] float64; lse: [n_seq, 16] or
- * NULL. Returns 0 on success, -1 for an out-of-range row index, -3 for bad
- * arguments.
+ * Full decode over a paged KV buffer for the sequences listed in seq_ids (all
+ * B sequences, in order, when seq_ids is NULL). kv_indptr [B+1] counts pages,
+ * kv_indices holds page ids, kv_last_page_len [B] the tokens used in each
+ * last page (NULL: every last page is full); num_rows = num_pages * page_size.
+ * out: [n_seq, 16, 512] float64; lse: [n_seq, 16] or NULL. Returns 0 on
+ * success, -1 for a token row outside the buffer, -3 for bad arguments.
  */
-int oracle_decode(int batch, const uint16_t* q, const void* kv, int64_t num_slots, int mode, float kv_scale,
-                  const int32_t* kv_indptr, const int32_t* kv_indices, double sm_scale, const int32_t* seq_ids,
-                  int n_seq, double* out, double* lse) {
+int oracle_decode_paged(int batch, const uint16_t* q, const void* kv, int64_t num_rows, int mode, float kv_scale,
+                        const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                        int page_size, double sm_scale, const int32_t* seq_ids, int n_seq, double* out,
+                        double* lse) {
   int i, bad = 0;
-  if (batch < 0 || mode < 0 || mode > 2 || !out) return -3;
+  if (batch < 0 || mode < 0 || mode > 2 || page_size < 1 || !out) return -3;
   if (!seq_ids) n_seq = batch;
   for (i = 0; i < n_seq; ++i) {
     int b = seq_ids ? seq_ids[i] : i;
-    if (b < 0 || b >= batch || kv_indptr[b + 1] < kv_indptr[b]) return -3;
+    if (b < 0 || b >= batch || seq_tokens(kv_indptr, kv_last_page_len, page_size, b) < 0) return -3;
   }
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (i = 0; i < n_seq * ORACLE_HEADS; ++i) {
     int k = i / ORACLE_HEADS, h = i % ORACLE_HEADS;
     int b = seq_ids ? seq_ids[k] : k;
     double l;
-    int rc = attend_head(q, kv, num_slots, mode, (double)kv_scale, kv_indptr, kv_indices, sm_scale, b, h, 0,
-                         (int64_t)kv_indptr[b + 1] - kv_indptr[b], out + (size_t)i * ORACLE_V_DIM, &l);
+    int rc = attend_head(q, kv, num_rows, mode, (double)kv_scale, kv_indptr, kv_indices, page_size, sm_scale, b, h, 0,
+                         seq_tokens(kv_indptr, kv_last_page_len, page_size, b), out + (size_t)i * ORACLE_V_DIM, &l);
     if (rc) bad |= 1;
     if (lse) lse[i] = l;
   }
   return bad ? -1 : 0;
+}
+
+/* The unpaged decode: page_size 1, so kv_indptr / kv_indices address single rows. */
+int oracle_decode(int batch, const uint16_t* q, const void* kv, int64_t num_slots, int mode, float kv_scale,
+                  const int32_t* kv_indptr, const int32_t* kv_indices, double sm_scale, const int32_t* seq_ids,
+                  int n_seq, double* out, double* lse) {
+  return oracle_decode_paged(batch, q, kv, num_slots, mode, kv_scale, kv_indptr, kv_indices, NULL, 1, sm_scale,
+                             seq_ids, n_seq, out, lse);
 }
 
 /*
@@ -209,7 +246,7 @@ int oracle_decode_range(int batch, const uint16_t* q, const void* kv, int64_t nu
   len = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
   if (t_begin < 0 || t_end > len || t_begin > t_end) return -3;
   for (h = 0; h < ORACLE_HEADS; ++h)
-    if (attend_head(q, kv, num_slots, mode, (double)kv_scale, kv_indptr, kv_indices, sm_scale, b, h, t_begin, t_end,
+    if (attend_head(q, kv, num_slots, mode, (double)kv_scale, kv_indptr, kv_indices, 1, sm_scale, b, h, t_begin, t_end,
                     out + (size_t)h * ORACLE_V_DIM, lse + h))
       bad = 1;
   return bad ? -1 : 0;

@@ -236,8 +236,126 @@ def pin_empty_and_errors(lib):
     raise AssertionError("out-of-range row index was not reported")
 
 
+# ---------------------------------------------------------------- paged layout
+
+def _paged(lengths, ps, mode, seed, **kw):
+    return mi.make_paged_inputs(lengths, ps, mode, seed, **kw)
+
+
+def _dec_paged(inp, lib, **kw):
+    return oracle.decode_paged(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, inp.kv_last_page_len, inp.page_size,
+                               inp.sm_scale, inp.mode, inp.kv_scale, lib=lib, **kw)
+
+
+def sdpa_reference_paged(inp: mi.Inputs, lengths):
+    """torch float64 SDPA over each sequence's tokens, gathered by viewing the buffer as
+    [num_pages, page_size, 576] (the pages' own view), indexing it with the page ids and
+    keeping the first L_b rows (``lengths`` are the generator's token counts)."""
+    kvv = _torch_kv_values(inp)
+    pages = kvv.view(-1, inp.page_size, D)
+    qv = _torch_q_values(inp)
+    ip = inp.kv_indptr.tolist()
+    outs, lses = [], []
+    for b, L in enumerate(lengths):
+        if L == 0:
+            outs.append(torch.zeros(H, DV, dtype=torch.float64))
+            lses.append(torch.full((H,), -math.inf, dtype=torch.float64))
+            continue
+        ids = inp.kv_indices[ip[b]:ip[b + 1]].long()
+        k = pages[ids].reshape(-1, D)[:L]
+        qb = qv[b]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qb[None, :, None, :], k[None, None].expand(1, H, -1, -1),
+            k[None, None, :, :DV].expand(1, H, -1, -1), scale=inp.sm_scale)[0, :, 0, :]
+        outs.append(o)
+        lses.append(torch.logsumexp((qb @ k.T) * inp.sm_scale, dim=1))
+    return torch.stack(outs).numpy(), torch.stack(lses).numpy()
+
+
+def pin_paged_library_sdpa(lib):
+    """Paged buffers (ragged last pages, shuffled page order, unused pages) against torch
+    SDPA over the tokens gathered through the [pages, page_size, 576] view, all modes."""
+    cases = [([1, 9, 16, 0, 37], 8), ([3, 4, 1, 12], 2), ([33, 64, 5], 16), ([7, 2], 3)]
+    for k, (lengths, ps) in enumerate(cases):
+        for mode in (0, 1, 2):
+            inp = _paged(lengths, ps, mode, seed=40 + 3 * k + mode, permute=True, extra_pages=3, q_std=2.0)
+            out, lse = _dec_paged(inp, lib)
+            ref, ref_lse = sdpa_reference_paged(inp, lengths)
+            np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(lse, ref_lse, rtol=1e-11, atol=1e-12)
+
+
+def pin_paged_unit_pages(lib):
+    """page_size 1 with full last pages is the row-addressed decode."""
+    inp = _inputs([1, 6, 17], 1, seed=12, permute=True, extra_slots=4)
+    out, lse = _dec(inp, lib)
+    ones = torch.ones(inp.batch, dtype=torch.int32)
+    out2, lse2 = oracle.decode_paged(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, ones, 1, inp.sm_scale, 1,
+                                     inp.kv_scale, lib=lib)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def pin_paged_permutation(lib):
+    """Moving whole pages to other page slots (and their ids with them) leaves O unchanged."""
+    for mode in (0, 1):
+        inp = _paged([13, 29, 8], 4, mode, seed=5, extra_pages=2)
+        out, lse = _dec_paged(inp, lib)
+        n_pages = inp.kv.shape[0] // 4
+        perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(4))
+        inv = torch.argsort(perm)
+        kv_moved = inp.kv.view(n_pages, 4, D)[perm].reshape(-1, D).contiguous()
+        moved = mi.Inputs(inp.mode, inp.q, kv_moved, inp.kv_scale, inp.kv_indptr,
+                          inv[inp.kv_indices.long()].to(torch.int32), inp.sm_scale, 4, inp.kv_last_page_len)
+        out2, lse2 = _dec_paged(moved, lib)
+        np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse2, lse, rtol=1e-12, atol=1e-13)
+
+
+def pin_paged_unused_rows_ignored(lib):
+    """Rows past a sequence's last used token (the rest of its last page, and unused pages)
+    do not enter the result: overwriting them with extreme values changes nothing."""
+    for mode in (0, 1):
+        lengths, ps = [5, 16, 11], 8
+        inp = _paged(lengths, ps, mode, seed=6, extra_pages=2)
+        out, lse = _dec_paged(inp, lib)
+        used = torch.zeros(inp.kv.shape[0], dtype=torch.bool)
+        ip = inp.kv_indptr.tolist()
+        for b, L in enumerate(lengths):
+            for t in range(L):
+                used[int(inp.kv_indices[ip[b] + t // ps]) * ps + t % ps] = True
+        assert int(used.sum()) == sum(lengths)
+        big = inp.kv.clone()
+        big[~used] = (torch.tensor(3.0e4, dtype=torch.bfloat16) if mode == 0
+                      else torch.tensor(0x7E, dtype=torch.uint8))
+        out2, lse2 = _dec_paged(mi.Inputs(inp.mode, inp.q, big, inp.kv_scale, inp.kv_indptr, inp.kv_indices,
+                                          inp.sm_scale, ps, inp.kv_last_page_len), lib)
+        assert np.array_equal(out2, out) and np.array_equal(lse2, lse)
+
+
+def pin_paged_errors(lib):
+    """A last page length outside [1, page_size], or a page id past the buffer, is reported."""
+    inp = _paged([5, 9], 4, 0, seed=7)
+    for bad_last in (0, 5):
+        lp = inp.kv_last_page_len.clone()
+        lp[1] = bad_last
+        try:
+            oracle.decode_paged(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, lp, 4, inp.sm_scale, 0, lib=lib)
+        except ValueError:
+            continue
+        raise AssertionError(f"last page length {bad_last} was not reported")
+    ix = inp.kv_indices.clone()
+    ix[-1] = inp.kv.shape[0] // 4
+    try:
+        oracle.decode_paged(inp.q, inp.kv, inp.kv_indptr, ix, inp.kv_last_page_len, 4, inp.sm_scale, 0, lib=lib)
+    except ValueError:
+        return
+    raise AssertionError("page id past the buffer was not reported")
+
+
 ALL_PINS = [
     pin_bf16_decode, pin_e4m3_decode_table, pin_e4m3_encode_vs_torch, pin_e4m3_encode_saturates,
     pin_single_row, pin_identical_rows, pin_uniform_scores, pin_two_rows, pin_convex_hull,
     pin_permutation, pin_library_sdpa, pin_split_combine, pin_empty_and_errors,
+    pin_paged_library_sdpa, pin_paged_unit_pages, pin_paged_permutation, pin_paged_unused_rows_ignored,
+    pin_paged_errors,
 ]

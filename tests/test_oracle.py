@@ -32,7 +32,10 @@ MUTANTS = {
     "missing_normalisation": ("double w = s[t] / z;", "double w = s[t];"),
     "missing_sm_scale": ("s[t] = sm_scale * acc;", "s[t] = acc;"),
     "wrong_head": ("((int64_t)b * ORACLE_HEADS + h) * ORACLE_QK_DIM", "((int64_t)b * ORACLE_HEADS + 0) * ORACLE_QK_DIM"),
-    "indices_ignored": ("int64_t row = kv_indices[base + t_begin + t];", "int64_t row = base + t_begin + t;"),
+    "indices_ignored": ("return (int64_t)kv_indices[page_base + t / page_size] * page_size + t % page_size;",
+                        "return page_base * page_size + t;"),
+    "page_offset_dropped": ("* page_size + t % page_size;", "* page_size;"),
+    "last_page_len_ignored": ("return (pages - 1) * page_size + last;", "return pages * page_size;"),
     "lse_missing_max": ("*lse = m + log(z);", "*lse = log(z);"),
     "combine_unnormalised": ("double w = exp(part_lse[s * ORACLE_HEADS + h] - m) / z;",
                              "double w = exp(part_lse[s * ORACLE_HEADS + h] - m);"),
