@@ -9,7 +9,8 @@
  *   s_t      = sm_scale * <q[b,h,:], kv[row_t,:]>            (all 576 dims)
  *   out[b,h] = sum_t softmax_t(s) * kv[row_t, 0:512]          (first 512 dims)
  * with row_t = kv_indices[kv_indptr[b] + t] for 0 <= t < kv_indptr[b+1] -
- * kv_indptr[b] (page_size = 1: every page is one row). The pages' V6c and
+ * kv_indptr[b] (page_size = 1: every page is one row; mla_decode_paged takes
+ * pages of several rows). The pages' V6c and
  * v86 submissions run it as a persistent stage-1 kernel over a precomputed
  * work list followed by a split reduce (submission 690201 "V6c",
  * custom_kernel: direct stage1 and reduce calls; _build_cache: metadata and
@@ -40,7 +41,7 @@ extern "C" {
 #define MLA_NUM_KV_HEADS 1
 #define MLA_QK_HEAD_DIM 576
 #define MLA_V_HEAD_DIM 512
-#define MLA_PAGE_SIZE 1
+#define MLA_PAGE_SIZE 1 /* the row-addressed layout of mla_decode; mla_decode_paged takes any page size */
 
 /* Value modes (dtype_mode argument). */
 enum mla_dtype_mode {
@@ -245,6 +246,51 @@ int mla_decode_noalloc(const void* q, const void* kv, const float* kv_scale, con
                        const int32_t* kv_indptr, const int32_t* kv_indices, int batch, int64_t num_kv_slots,
                        void* out, float sm_scale, int dtype_mode, int* status_dev, void* stream);
 
+/*
+ * Paged KV layout (kernelbot amd-mixed-mla submission 641982 "v86",
+ * _run_a8w8, and 598454 "v12", custom_kernel: the KV buffer viewed as
+ * [num_pages, page_size, 1, 576], kv_indptr // page_size, page ids in
+ * kv_indices, kv_last_page_lens). Sequence b owns pages
+ * kv_indices[kv_indptr[b] .. kv_indptr[b+1]); its last page holds
+ * kv_last_page_len[b] tokens (1 <= len <= page_size), every other page holds
+ * page_size. Token t is row kv_indices[kv_indptr[b] + t / page_size] *
+ * page_size + t % page_size of the buffer. The rows of a last page past its
+ * length are never read into the result.
+ *
+ * mla_decode_plan_paged — the planner for that layout.
+ *   kv_indptr_host        host int32 [B+1] page offsets (0 first, non-decreasing).
+ *   kv_last_page_len_host host int32 [B] (may be NULL when page_size is 1).
+ *   page_size             tokens per page (>= 1).
+ *   options->num_kv_slots counts ROWS of the buffer (num_pages * page_size).
+ * Plans are cached by layout as well; a paged plan serves only
+ * mla_decode_paged with the same page_size (any other decode call returns
+ * MLA_ERR_ARG). Errors as mla_decode_plan, plus MLA_ERR_INDPTR for a last page
+ * length outside [1, page_size] or a sequence longer than 2^31 - 1 tokens.
+ */
+int mla_decode_plan_paged(int batch, const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                          int page_size, int num_sms, const mla_plan_options* options, mla_plan** plan_out);
+/*
+ * mla_decode_paged — mla_decode over the paged layout.
+ *   kv               device [num_pages * page_size, 576] (bf16 or e4m3 bytes).
+ *   kv_indptr        device int32 [B+1] page offsets, equal to the plan's.
+ *   kv_indices       device int32 page ids.
+ *   kv_last_page_len device int32 [B], equal to the plan's (may be NULL when
+ *                    page_size is 1). The kernel recomputes every token count it
+ *                    touches and records MLA_ERR_PLAN_MISMATCH, skipping that work,
+ *                    when it differs from the plan's.
+ *   page_size        must equal the plan's.
+ * Other arguments, ownership, ordering and errors as for mla_decode. A page id
+ * whose rows fall outside [0, num_kv_slots) (when the plan was given the pool
+ * size) is read as zeros and recorded as MLA_ERR_INDEX.
+ */
+int mla_decode_paged(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+                     const int32_t* kv_indices, const int32_t* kv_last_page_len, int page_size, void* out,
+                     float sm_scale, int dtype_mode, mla_plan* workspace, void* stream);
+/* mla_plan_compute_host for the paged layout (same outputs; token offsets in items). */
+int mla_plan_compute_host_paged(int batch, const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                                int page_size, int num_sms, const mla_plan_options* options, int32_t* counts,
+                                int32_t* items, int items_cap, int32_t* work_indptr, int indptr_cap,
+                                int32_t* reduce, int reduce_cap);
 /* Human-readable name of a status code (static string). */
 const char* mla_strerror(int status);
 

@@ -40,7 +40,8 @@ STATUS = {
 EXPORTS = (
     "mla_decode_plan", "mla_decode_plan_ex", "mla_plan_release", "mla_plan_get_info", "mla_decode",
     "mla_decode_stage1", "mla_decode_reduce", "mla_plan_check_error", "mla_strerror", "mla_version",
-    "mla_plan_compute_host", "mla_decode_noalloc",
+    "mla_plan_compute_host", "mla_decode_noalloc", "mla_decode_plan_paged", "mla_decode_paged",
+    "mla_plan_compute_host_paged",
 )
 
 
@@ -94,6 +95,10 @@ def load_library(path: str | None = None):
         lib.mla_version.argtypes = []
         lib.mla_plan_compute_host.argtypes = [I, V, I, ctypes.POINTER(PlanOptions), V, V, I, V, I, V, I]
         lib.mla_decode_noalloc.argtypes = [V, V, V, V, V, V, I, I64, V, F, I, V, V]
+        lib.mla_decode_plan_paged.argtypes = [I, V, V, I, I, ctypes.POINTER(PlanOptions), ctypes.POINTER(V)]
+        lib.mla_decode_paged.argtypes = [V, V, V, V, V, V, I, V, F, I, V, V]
+        lib.mla_plan_compute_host_paged.argtypes = [I, V, V, I, I, ctypes.POINTER(PlanOptions), V, V, I, V, I, V,
+                                                    I]
         for name in EXPORTS:
             if name not in ("mla_strerror",):
                 getattr(lib, name).restype = I
@@ -125,17 +130,32 @@ def _host_indptr(kv_indptr) -> torch.Tensor:
 
 
 class Plan:
-    """A split-KV plan (work list, reduce map and partial workspace) owned by the library."""
+    """A split-KV plan (work list, reduce map and partial workspace) owned by the library.
 
-    def __init__(self, kv_indptr_host, num_sms: int = 0, **options):
+    With ``page_size`` given the plan is for the paged layout (kv_indptr counts
+    pages, ``kv_last_page_len_host`` the tokens of each last page) and serves
+    decode_paged only.
+    """
+
+    def __init__(self, kv_indptr_host, num_sms: int = 0, *, page_size: int | None = None,
+                 kv_last_page_len_host=None, **options):
         lib = load_library()
         ip = _host_indptr(kv_indptr_host)
         self.batch = ip.numel() - 1
         self._lib = lib
         self._handle = ctypes.c_void_p()
         o = _opts(**options)
-        _check(lib.mla_decode_plan_ex(self.batch, ip.data_ptr(), int(num_sms), ctypes.byref(o),
-                                      ctypes.byref(self._handle)), "mla_decode_plan")
+        self.paged = page_size is not None
+        self.page_size = int(page_size) if self.paged else 1
+        if self.paged:
+            lp = None if kv_last_page_len_host is None else _host_indptr(kv_last_page_len_host)
+            _check(lib.mla_decode_plan_paged(self.batch, ip.data_ptr(), None if lp is None else lp.data_ptr(),
+                                             self.page_size, int(num_sms), ctypes.byref(o),
+                                             ctypes.byref(self._handle)), "mla_decode_plan_paged")
+            self.kv_last_page_len_host = lp
+        else:
+            _check(lib.mla_decode_plan_ex(self.batch, ip.data_ptr(), int(num_sms), ctypes.byref(o),
+                                          ctypes.byref(self._handle)), "mla_decode_plan")
         self.kv_indptr_host = ip
 
     @property
@@ -166,6 +186,13 @@ class Plan:
 def plan(kv_indptr_host, num_sms: int = 0, **options) -> Plan:
     """Build (or fetch from the library's cache) the plan for this batch layout."""
     return Plan(kv_indptr_host, num_sms, **options)
+
+
+def plan_paged(kv_indptr_host, kv_last_page_len_host, page_size: int, num_sms: int = 0, **options) -> Plan:
+    """Plan for the paged layout: kv_indptr in pages of ``page_size`` tokens,
+    ``kv_last_page_len_host`` [B] the tokens used in each sequence's last page."""
+    return Plan(kv_indptr_host, num_sms, page_size=page_size, kv_last_page_len_host=kv_last_page_len_host,
+                **options)
 
 
 def _stream_ptr(stream) -> int | None:
@@ -226,6 +253,30 @@ def decode(q, kv, kv_scale, kv_indptr, kv_indices, out=None, *, sm_scale: float 
     return out
 
 
+def decode_paged(q, kv, kv_scale, kv_indptr, kv_indices, kv_last_page_len, page_size: int, out=None, *,
+                 sm_scale: float = SM_SCALE, dtype_mode=None, plan: Plan | None = None, stream=None,
+                 validate: bool = True) -> torch.Tensor:
+    """MLA decode over the paged layout: kv [num_pages * page_size, 576], kv_indptr
+    int32 [B+1] page offsets, kv_indices int32 page ids and kv_last_page_len int32
+    [B] on the device. Without ``plan`` one is built from host copies."""
+    mode = _mode_of(kv) if dtype_mode is None else int(dtype_mode)
+    p = plan if plan is not None else plan_paged(kv_indptr, kv_last_page_len, page_size, num_kv_slots=kv.shape[0])
+    if out is None:
+        out = torch.empty((p.batch, HEADS, V_DIM), dtype=torch.bfloat16, device=q.device)
+    if validate:
+        _validate(q, kv, kv_scale, kv_indptr, kv_indices, out, mode, p)
+        if page_size > 1 and (kv_last_page_len is None or kv_last_page_len.dtype != torch.int32
+                              or not kv_last_page_len.is_cuda or kv_last_page_len.numel() != p.batch):
+            raise ValueError("kv_last_page_len must be an int32 CUDA tensor [B]")
+    ks = kv_scale.data_ptr() if kv_scale is not None else None
+    lp = kv_last_page_len.data_ptr() if kv_last_page_len is not None else None
+    _check(load_library().mla_decode_paged(q.data_ptr(), kv.data_ptr(), ks, kv_indptr.data_ptr(),
+                                           kv_indices.data_ptr(), lp, int(page_size), out.data_ptr(),
+                                           float(sm_scale), int(mode), p.handle, _stream_ptr(stream)),
+           "mla_decode_paged")
+    return out
+
+
 def decode_stage1(q, kv, kv_scale, kv_indptr, kv_indices, out, *, plan: Plan, sm_scale: float = SM_SCALE,
                   dtype_mode=None, stream=None) -> torch.Tensor:
     """Only the persistent stage-1 kernel (final rows of unsplit sequences + partials)."""
@@ -260,6 +311,33 @@ def plan_compute_host(kv_indptr_host, num_sms: int, **options) -> dict:
     _check(lib.mla_plan_compute_host(batch, ip.data_ptr(), int(num_sms), ctypes.byref(o), counts.ctypes.data,
                                      items.ctypes.data, items.shape[0], wip.ctypes.data, wip.shape[0],
                                      red.ctypes.data, red.shape[0]), "mla_plan_compute_host")
+    return {"items": items[:n_items], "work_indptr": wip, "reduce": red[:n_reduce], "num_ctas": n_ctas,
+            "num_slots": n_slots}
+
+
+def plan_compute_host_paged(kv_indptr_host, kv_last_page_len_host, page_size: int, num_sms: int,
+                            **options) -> dict:
+    """plan_compute_host for the paged layout (item offsets are tokens)."""
+    import numpy as np
+
+    lib = load_library()
+    ip = _host_indptr(kv_indptr_host)
+    lp = None if kv_last_page_len_host is None else _host_indptr(kv_last_page_len_host)
+    lpp = None if lp is None else lp.data_ptr()
+    batch = ip.numel() - 1
+    o = _opts(**options)
+    counts = np.zeros(4, dtype=np.int32)
+    _check(lib.mla_plan_compute_host_paged(batch, ip.data_ptr(), lpp, int(page_size), int(num_sms), ctypes.byref(o),
+                                           counts.ctypes.data, None, 0, None, 0, None, 0),
+           "mla_plan_compute_host_paged")
+    n_items, n_ctas, n_slots, n_reduce = (int(x) for x in counts)
+    items = np.zeros((max(n_items, 1), 5), dtype=np.int32)
+    wip = np.zeros(n_ctas + 1, dtype=np.int32)
+    red = np.zeros((max(n_reduce, 1), 3), dtype=np.int32)
+    _check(lib.mla_plan_compute_host_paged(batch, ip.data_ptr(), lpp, int(page_size), int(num_sms), ctypes.byref(o),
+                                           counts.ctypes.data, items.ctypes.data, items.shape[0], wip.ctypes.data,
+                                           wip.shape[0], red.ctypes.data, red.shape[0]),
+           "mla_plan_compute_host_paged")
     return {"items": items[:n_items], "work_indptr": wip, "reduce": red[:n_reduce], "num_ctas": n_ctas,
             "num_slots": n_slots}
 

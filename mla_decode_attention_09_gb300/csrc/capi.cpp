@@ -17,7 +17,10 @@ struct mla_plan {
   int batch = 0;
   int num_sms = 0;
   mla::PlanOptions opt;
+  bool paged = false;            // built by mla_decode_plan_paged: serves mla_decode_paged only
+  int page_size = 1;
   std::vector<int32_t> indptr;   // cache key contents
+  std::vector<int32_t> last_page_len;
   mla::HostPlan host;
   mla::DevicePlan dev{};
   void* block = nullptr;         // single device allocation backing every buffer
@@ -32,13 +35,25 @@ std::vector<mla_plan*> g_cache;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, int num_sms,
+// Layout a plan is built for: row addressing, or pages of page_size tokens
+// with the last page lengths `last` (NULL when page_size is 1).
+struct Layout {
+  bool paged;
+  int page_size;
+  const int32_t* last;
+};
+
+bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, const Layout& l, int num_sms,
               const mla::PlanOptions& o) {
-  return p->device == device && p->batch == batch && p->num_sms == num_sms &&
-         p->opt.num_kv_slots == o.num_kv_slots && p->opt.min_rows_per_split == o.min_rows_per_split &&
-         p->opt.granularity == o.granularity && p->opt.ctas_per_sm == o.ctas_per_sm &&
-         p->opt.fp8_kernel == o.fp8_kernel &&
-         std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0;
+  if (!(p->device == device && p->batch == batch && p->num_sms == num_sms && p->paged == l.paged &&
+        p->page_size == l.page_size && p->opt.num_kv_slots == o.num_kv_slots &&
+        p->opt.min_rows_per_split == o.min_rows_per_split && p->opt.granularity == o.granularity &&
+        p->opt.ctas_per_sm == o.ctas_per_sm && p->opt.fp8_kernel == o.fp8_kernel &&
+        std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0))
+    return false;
+  if (p->last_page_len.empty() != (l.last == nullptr || batch == 0)) return false;
+  return l.last == nullptr || batch == 0 ||
+         std::memcmp(p->last_page_len.data(), l.last, sizeof(int32_t) * (size_t)batch) == 0;
 }
 
 void destroy_plan(mla_plan* p) {
@@ -65,16 +80,20 @@ int check_device(int* device_out) {
   return MLA_OK;
 }
 
-int make_plan(int batch, const int32_t* kv_indptr_host, int num_sms, const mla::PlanOptions& opt, int device,
-              mla_plan** out) {
+int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num_sms, const mla::PlanOptions& opt,
+              int device, mla_plan** out) {
   mla_plan* p = new (std::nothrow) mla_plan();
   if (!p) return MLA_ERR_NOMEM;
   p->device = device;
   p->batch = batch;
   p->num_sms = num_sms;
   p->opt = opt;
+  p->paged = l.paged;
+  p->page_size = l.page_size;
   p->indptr.assign(kv_indptr_host, kv_indptr_host + batch + 1);
-  int rc = mla::build_host_plan(batch, kv_indptr_host, num_sms, opt, &p->host);
+  if (l.last && batch > 0) p->last_page_len.assign(l.last, l.last + batch);
+  int rc = l.paged ? mla::build_host_plan_paged(batch, kv_indptr_host, l.last, l.page_size, num_sms, opt, &p->host)
+                   : mla::build_host_plan(batch, kv_indptr_host, num_sms, opt, &p->host);
   if (rc != MLA_OK) {
     delete p;
     return rc;
@@ -131,8 +150,11 @@ int make_plan(int batch, const int32_t* kv_indptr_host, int num_sms, const mla::
 }
 
 int validate_decode(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
-                    const int32_t* kv_indices, const void* out, int dtype_mode, const mla_plan* plan) {
+                    const int32_t* kv_indices, const void* out, int dtype_mode, const mla_plan* plan,
+                    const Layout& l) {
   if (!plan || plan->refcount <= 0) return MLA_ERR_ARG;
+  if (plan->paged != l.paged || plan->page_size != l.page_size) return MLA_ERR_ARG;
+  if (l.paged && l.page_size > 1 && plan->batch > 0 && !l.last) return MLA_ERR_ARG;
   if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8) return MLA_ERR_DTYPE;
   if (plan->batch > 0) {
     if (!q || !kv || !kv_indptr || !out) return MLA_ERR_ARG;
@@ -146,14 +168,11 @@ int validate_decode(const void* q, const void* kv, const float* kv_scale, const 
   return MLA_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
-                       mla_plan** plan_out) {
+int plan_common(int batch, const int32_t* kv_indptr_host, const Layout& layout, int num_sms,
+                const mla_plan_options* options, mla_plan** plan_out) {
   try {
     if (!plan_out || batch < 0 || (!kv_indptr_host && batch > 0)) return MLA_ERR_ARG;
+    if (layout.page_size < 1 || (layout.page_size > 1 && batch > 0 && !layout.last)) return MLA_ERR_ARG;
     *plan_out = nullptr;
     int device = -1;
     int rc = check_device(&device);
@@ -167,14 +186,14 @@ int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, co
     const int32_t* indptr = batch > 0 ? kv_indptr_host : &kZero;
     std::lock_guard<std::mutex> lock(g_mu);
     for (mla_plan* p : g_cache) {
-      if (same_key(p, device, batch, indptr, num_sms, opt)) {
+      if (same_key(p, device, batch, indptr, layout, num_sms, opt)) {
         ++p->refcount;
         *plan_out = p;
         return MLA_OK;
       }
     }
     mla_plan* p = nullptr;
-    rc = make_plan(batch, indptr, num_sms, opt, device, &p);
+    rc = make_plan(batch, indptr, layout, num_sms, opt, device, &p);
     if (rc != MLA_OK) return rc;
     g_cache.push_back(p);
     *plan_out = p;
@@ -182,6 +201,32 @@ int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, co
   } catch (...) {
     return MLA_ERR_NOMEM;
   }
+}
+
+int decode_common(const mla::DecodeArgs& a, int dtype_mode, mla_plan* workspace, void* stream, bool reduce) {
+  if (workspace->batch == 0) return MLA_OK;
+  if (mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream) != 0) return MLA_ERR_CUDA;
+  // the reduce is launched programmatically dependent: it starts while stage 1
+  // drains and waits for its results on the device
+  if (reduce && mla::launch_reduce(a.out, workspace->dev, stream, true) != 0) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+constexpr Layout kRows{false, 1, nullptr};
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
+                       mla_plan** plan_out) {
+  return plan_common(batch, kv_indptr_host, kRows, num_sms, options, plan_out);
+}
+
+int mla_decode_plan_paged(int batch, const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                          int page_size, int num_sms, const mla_plan_options* options, mla_plan** plan_out) {
+  const Layout l{true, page_size, page_size > 1 ? kv_last_page_len_host : nullptr};
+  return plan_common(batch, kv_indptr_host, l, num_sms, options, plan_out);
 }
 
 int mla_decode_plan(int batch, const int32_t* kv_indptr_host, int num_sms, mla_plan** plan_out) {
@@ -220,12 +265,10 @@ int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
 int mla_decode_stage1(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
                       const int32_t* kv_indices, void* out, float sm_scale, int dtype_mode, mla_plan* workspace,
                       void* stream) {
-  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace);
+  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace, kRows);
   if (rc != MLA_OK) return rc;
-  if (workspace->batch == 0) return MLA_OK;
   const mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
-  return mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream) == 0 ? MLA_OK
-                                                                                             : MLA_ERR_CUDA;
+  return decode_common(a, dtype_mode, workspace, stream, false);
 }
 
 int mla_decode_reduce(void* out, mla_plan* workspace, void* stream) {
@@ -239,15 +282,23 @@ int mla_decode_reduce(void* out, mla_plan* workspace, void* stream) {
 int mla_decode(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
                const int32_t* kv_indices, void* out, float sm_scale, int dtype_mode, mla_plan* workspace,
                void* stream) {
-  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace);
+  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace, kRows);
   if (rc != MLA_OK) return rc;
-  if (workspace->batch == 0) return MLA_OK;
   const mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
-  if (mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream) != 0) return MLA_ERR_CUDA;
-  // the reduce is launched programmatically dependent: it starts while stage 1
-  // drains and waits for its results on the device
-  if (mla::launch_reduce(out, workspace->dev, stream, true) != 0) return MLA_ERR_CUDA;
-  return MLA_OK;
+  return decode_common(a, dtype_mode, workspace, stream, true);
+}
+
+int mla_decode_paged(const void* q, const void* kv, const float* kv_scale, const int32_t* kv_indptr,
+                     const int32_t* kv_indices, const int32_t* kv_last_page_len, int page_size, void* out,
+                     float sm_scale, int dtype_mode, mla_plan* workspace, void* stream) {
+  if (page_size < 1) return MLA_ERR_ARG;
+  const Layout l{true, page_size, page_size > 1 ? kv_last_page_len : nullptr};
+  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace, l);
+  if (rc != MLA_OK) return rc;
+  mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
+  a.kv_last_page_len = l.last;
+  a.page_size = page_size;
+  return decode_common(a, dtype_mode, workspace, stream, true);
 }
 
 int mla_plan_check_error(mla_plan* plan, void* stream) {
@@ -264,14 +315,15 @@ const char* mla_strerror(int status) {
     case MLA_OK: return "ok";
     case MLA_ERR_ARG: return "invalid argument";
     case MLA_ERR_DTYPE: return "unknown dtype_mode";
-    case MLA_ERR_PLAN_MISMATCH: return "device kv_indptr does not match the plan";
+    case MLA_ERR_PLAN_MISMATCH: return "device kv_indptr (or last page lengths) does not match the plan";
     case MLA_ERR_CUDA: return "CUDA runtime error";
     case MLA_ERR_TIMEOUT: return "a bounded wait in a kernel timed out";
     case MLA_ERR_ALIGN: return "q, kv or out is not 16-byte aligned";
     case MLA_ERR_NOMEM: return "allocation failed";
     case MLA_ERR_INDEX: return "kv_indices entry out of range";
     case MLA_ERR_DEVICE: return "no usable sm_103 device or wrong device for the plan";
-    case MLA_ERR_INDPTR: return "kv_indptr must start at 0 and be non-decreasing";
+    case MLA_ERR_INDPTR:
+      return "kv_indptr must start at 0 and be non-decreasing (and last page lengths lie in [1, page_size])";
     case MLA_ERR_NOALLOC_LIMIT:
       return "request exceeds the fixed scratch of mla_decode_noalloc (batch <= 1024, <= 500 partial slots)";
     default: return "unknown status";
@@ -282,6 +334,33 @@ int mla_version(void) { return 100; }
 
 // Host-only view of the planner (no CUDA call): fills caller arrays with the
 // work list the plan would hold. Any output pointer may be NULL to only count.
+static int export_host_plan(int rc, mla::HostPlan& h, int32_t* counts4, int32_t* items5, int items_cap,
+                            int32_t* work_indptr, int indptr_cap, int32_t* reduce3, int reduce_cap) {
+  if (rc != MLA_OK) return rc;
+  counts4[0] = h.n_items;
+  counts4[1] = h.num_ctas;
+  counts4[2] = h.num_slots;
+  counts4[3] = h.n_reduce;
+  if (items5 && items_cap >= h.n_items)
+    for (int i = 0; i < h.n_items; ++i) {
+      items5[5 * i + 0] = h.items[i].b;
+      items5[5 * i + 1] = h.items[i].t_begin;
+      items5[5 * i + 2] = h.items[i].t_end;
+      items5[5 * i + 3] = h.items[i].slot;
+      items5[5 * i + 4] = h.items[i].seq_len;
+    }
+  if (work_indptr && indptr_cap >= h.num_ctas + 1)
+    std::memcpy(work_indptr, h.work_indptr, sizeof(int32_t) * (size_t)(h.num_ctas + 1));
+  if (reduce3 && reduce_cap >= h.n_reduce)
+    for (int i = 0; i < h.n_reduce; ++i) {
+      reduce3[3 * i + 0] = h.reduce[i].b;
+      reduce3[3 * i + 1] = h.reduce[i].slot_begin;
+      reduce3[3 * i + 2] = h.reduce[i].n_slots;
+    }
+  mla::free_host_plan(&h);
+  return MLA_OK;
+}
+
 int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms, const mla_plan_options* options,
                           int32_t* counts4, int32_t* items5, int items_cap, int32_t* work_indptr, int indptr_cap,
                           int32_t* reduce3, int reduce_cap) {
@@ -289,31 +368,25 @@ int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms,
     if (!counts4) return MLA_ERR_ARG;
     mla::HostPlan h;
     static const int32_t kZero = 0;
-    int rc = mla::build_host_plan(batch, batch > 0 ? kv_indptr_host : &kZero, num_sms, mla::resolve_options(options),
-                                  &h);
-    if (rc != MLA_OK) return rc;
-    counts4[0] = h.n_items;
-    counts4[1] = h.num_ctas;
-    counts4[2] = h.num_slots;
-    counts4[3] = h.n_reduce;
-    if (items5 && items_cap >= h.n_items)
-      for (int i = 0; i < h.n_items; ++i) {
-        items5[5 * i + 0] = h.items[i].b;
-        items5[5 * i + 1] = h.items[i].t_begin;
-        items5[5 * i + 2] = h.items[i].t_end;
-        items5[5 * i + 3] = h.items[i].slot;
-        items5[5 * i + 4] = h.items[i].seq_len;
-      }
-    if (work_indptr && indptr_cap >= h.num_ctas + 1)
-      std::memcpy(work_indptr, h.work_indptr, sizeof(int32_t) * (size_t)(h.num_ctas + 1));
-    if (reduce3 && reduce_cap >= h.n_reduce)
-      for (int i = 0; i < h.n_reduce; ++i) {
-        reduce3[3 * i + 0] = h.reduce[i].b;
-        reduce3[3 * i + 1] = h.reduce[i].slot_begin;
-        reduce3[3 * i + 2] = h.reduce[i].n_slots;
-      }
-    mla::free_host_plan(&h);
-    return MLA_OK;
+    const int rc = mla::build_host_plan(batch, batch > 0 ? kv_indptr_host : &kZero, num_sms,
+                                        mla::resolve_options(options), &h);
+    return export_host_plan(rc, h, counts4, items5, items_cap, work_indptr, indptr_cap, reduce3, reduce_cap);
+  } catch (...) {
+    return MLA_ERR_NOMEM;
+  }
+}
+
+int mla_plan_compute_host_paged(int batch, const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                                int page_size, int num_sms, const mla_plan_options* options, int32_t* counts4,
+                                int32_t* items5, int items_cap, int32_t* work_indptr, int indptr_cap,
+                                int32_t* reduce3, int reduce_cap) {
+  try {
+    if (!counts4) return MLA_ERR_ARG;
+    mla::HostPlan h;
+    static const int32_t kZero = 0;
+    const int rc = mla::build_host_plan_paged(batch, batch > 0 ? kv_indptr_host : &kZero, kv_last_page_len_host,
+                                              page_size, num_sms, mla::resolve_options(options), &h);
+    return export_host_plan(rc, h, counts4, items5, items_cap, work_indptr, indptr_cap, reduce3, reduce_cap);
   } catch (...) {
     return MLA_ERR_NOMEM;
   }

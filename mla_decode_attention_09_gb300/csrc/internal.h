@@ -12,11 +12,11 @@ constexpr int kHeads = MLA_NUM_HEADS;     // 16 query heads share one KV head
 constexpr int kQkDim = MLA_QK_HEAD_DIM;   // 576 = 512 latent + 64 rope
 constexpr int kVDim = MLA_V_HEAD_DIM;     // 512: value = first 512 entries of the KV row
 
-// One unit of stage-1 work: rows [t_begin, t_end) of sequence b (row offsets
+// One unit of stage-1 work: tokens [t_begin, t_end) of sequence b (offsets
 // relative to the sequence start). slot >= 0: write normalised fp32 partial O
 // and LSE to workspace slot `slot`; slot < 0: the item covers the whole
-// sequence and writes final bf16 output. seq_len is the length the plan saw,
-// checked against the device kv_indptr.
+// sequence and writes final bf16 output. seq_len is the token count the plan
+// saw, checked against the device kv_indptr (and last page lengths).
 struct WorkItem {
   int32_t b;
   int32_t t_begin;
@@ -63,7 +63,12 @@ PlanOptions resolve_options(const mla_plan_options* o);
 
 // Pure host planning (no CUDA calls). Returns MLA_OK or an error; on success
 // the arrays in *out are malloc'ed and must be freed with free_host_plan.
+// Row addressing: sequence b holds kv_indptr[b+1] - kv_indptr[b] tokens.
 int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const PlanOptions& opt, HostPlan* out);
+// Paged addressing: kv_indptr counts pages of page_size tokens and
+// last_page_len[b] (1..page_size) gives the tokens used in b's last page.
+int build_host_plan_paged(int batch, const int32_t* kv_indptr, const int32_t* last_page_len, int page_size,
+                          int num_sms, const PlanOptions& opt, HostPlan* out);
 void free_host_plan(HostPlan* p);
 
 // Device-side view of a plan, passed to the kernels by value.
@@ -84,11 +89,35 @@ struct DecodeArgs {
   const void* q;
   const void* kv;
   const float* kv_scale;
-  const int32_t* kv_indptr;
-  const int32_t* kv_indices;
+  const int32_t* kv_indptr;   // per sequence: offsets into kv_indices (pages when page_size > 1)
+  const int32_t* kv_indices;  // KV row of each token, or page id of each page when page_size > 1
   void* out;
   float sm_scale;
+  const int32_t* kv_last_page_len = nullptr;  // [B], tokens used in each last page (page_size > 1)
+  int page_size = 1;                          // tokens per page; 1 = every kv_indices entry is a row
 };
+
+#ifdef __CUDACC__
+// Tokens of sequence b according to the device arrays: pages of page_size
+// tokens, the last one holding kv_last_page_len[b]. -1 when that length lies
+// outside [1, page_size] (the caller treats it like a plan mismatch).
+__device__ __forceinline__ int64_t device_seq_tokens(const DecodeArgs& a, int b) {
+  const int64_t pages = (int64_t)a.kv_indptr[b + 1] - a.kv_indptr[b];
+  if (a.page_size <= 1 || pages <= 0) return pages;
+  const int last = a.kv_last_page_len[b];
+  if (last < 1 || last > a.page_size) return -1;
+  return (pages - 1) * a.page_size + last;
+}
+// kv_indices position (relative to the sequence's first entry) of token t.
+__device__ __forceinline__ int token_entry(const DecodeArgs& a, int t) {
+  return a.page_size <= 1 ? t : t / a.page_size;
+}
+// KV row of token t given the kv_indices entry e that token_entry pointed at
+// (entry * page_size + t % page_size), in 64 bits: a caller range-checks it.
+__device__ __forceinline__ int64_t token_row(const DecodeArgs& a, int32_t e, int t) {
+  return a.page_size <= 1 ? (int64_t)e : (int64_t)e * a.page_size + t % a.page_size;
+}
+#endif
 
 // Kernel launchers (stage1.cu / reduce.cu). Return cudaError_t as int.
 int launch_stage1(int dtype_mode, const DecodeArgs& a, const DevicePlan& p, const void* zero_row, void* stream);

@@ -13,6 +13,8 @@
 // multiples of `granularity` rows from the sequence start, and no range is
 // shorter than `min_rows_per_split` unless the whole problem is.
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <utility>
 #include <cstdlib>
 #include <cstring>
@@ -42,17 +44,13 @@ void free_host_plan(HostPlan* p) {
   p->reduce = nullptr;
 }
 
-int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const PlanOptions& opt, HostPlan* out) {
-  if (batch < 0 || num_sms <= 0 || !out || (batch > 0 && !kv_indptr)) return MLA_ERR_ARG;
-  if (opt.granularity <= 0 || opt.min_rows_per_split <= 0 || opt.ctas_per_sm <= 0) return MLA_ERR_ARG;
-  *out = HostPlan{};
-  out->batch = batch;
-  if (batch > 0 && kv_indptr[0] != 0) return MLA_ERR_INDPTR;
-  int64_t total = 0;
-  for (int b = 0; b < batch; ++b) {
-    if (kv_indptr[b + 1] < kv_indptr[b]) return MLA_ERR_INDPTR;
-    total += (int64_t)kv_indptr[b + 1] - kv_indptr[b];
-  }
+namespace {
+
+// The planner proper, on the sequences' token counts laid end to end:
+// tok[b] is the first token of sequence b in that concatenation, tok[batch]
+// the total.
+int plan_tokens(int batch, const std::vector<int64_t>& tok, int num_sms, const PlanOptions& opt, HostPlan* out) {
+  const int64_t total = tok[(size_t)batch];
   out->total_rows = total;
 
   // Work is counted in granules: sequence b is ceil(L_b / G) granules of G
@@ -65,7 +63,7 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
   const int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
   std::vector<int64_t> gstart((size_t)batch + 1, 0);
   for (int b = 0; b < batch; ++b)
-    gstart[(size_t)b + 1] = gstart[(size_t)b] + ((int64_t)kv_indptr[b + 1] - kv_indptr[b] + G - 1) / G;
+    gstart[(size_t)b + 1] = gstart[(size_t)b] + (tok[(size_t)b + 1] - tok[(size_t)b] + G - 1) / G;
   const int64_t U = gstart[(size_t)batch];
   int64_t target = U > 0 ? (U + max_ctas - 1) / max_ctas : 1;
   target = std::max<int64_t>(target, (opt.min_rows_per_split + G - 1) / G);
@@ -81,7 +79,7 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
       const int mid = (lo + hi + 1) / 2;
       if (gstart[(size_t)mid] <= g) lo = mid; else hi = mid - 1;
     }
-    const int64_t S = kv_indptr[lo], L = (int64_t)kv_indptr[lo + 1] - S;
+    const int64_t S = tok[(size_t)lo], L = tok[(size_t)lo + 1] - S;
     cuts[(size_t)k] = S + std::min<int64_t>((g - gstart[(size_t)lo]) * G, L);
   }
   std::vector<std::pair<int64_t, int64_t>> ranges;  // non-empty CTA row ranges, in order
@@ -95,7 +93,7 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
   size_t cta = 0;
   const size_t last = ranges.size() - 1;
   for (int b = 0; b < batch; ++b) {
-    const int64_t S = kv_indptr[b], E = kv_indptr[b + 1];
+    const int64_t S = tok[(size_t)b], E = tok[(size_t)b + 1];
     while (cta < last && ranges[cta].second <= S) ++cta;
     if (S == E) {  // empty sequence: a zero-row item that writes zeros
       items.push_back(WorkItem{b, 0, 0, -1, 0, {0, 0, 0}});
@@ -154,6 +152,48 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
   std::memcpy(out->work_indptr, indptr.data(), sizeof(int32_t) * indptr.size());
   if (!reduce.empty()) std::memcpy(out->reduce, reduce.data(), sizeof(ReduceEntry) * reduce.size());
   return MLA_OK;
+}
+
+int check_common(int batch, const int32_t* kv_indptr, int num_sms, const PlanOptions& opt, HostPlan* out) {
+  if (batch < 0 || num_sms <= 0 || !out || (batch > 0 && !kv_indptr)) return MLA_ERR_ARG;
+  if (opt.granularity <= 0 || opt.min_rows_per_split <= 0 || opt.ctas_per_sm <= 0) return MLA_ERR_ARG;
+  *out = HostPlan{};
+  out->batch = batch;
+  if (batch > 0 && kv_indptr[0] != 0) return MLA_ERR_INDPTR;
+  for (int b = 0; b < batch; ++b)
+    if (kv_indptr[b + 1] < kv_indptr[b]) return MLA_ERR_INDPTR;
+  return MLA_OK;
+}
+
+}  // namespace
+
+int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const PlanOptions& opt, HostPlan* out) {
+  const int rc = check_common(batch, kv_indptr, num_sms, opt, out);
+  if (rc != MLA_OK) return rc;
+  std::vector<int64_t> tok((size_t)batch + 1, 0);
+  for (int b = 1; b <= batch; ++b) tok[(size_t)b] = kv_indptr[b];
+  return plan_tokens(batch, tok, num_sms, opt, out);
+}
+
+int build_host_plan_paged(int batch, const int32_t* kv_indptr, const int32_t* last_page_len, int page_size,
+                          int num_sms, const PlanOptions& opt, HostPlan* out) {
+  if (page_size < 1 || (batch > 0 && page_size > 1 && !last_page_len)) return MLA_ERR_ARG;
+  const int rc = check_common(batch, kv_indptr, num_sms, opt, out);
+  if (rc != MLA_OK) return rc;
+  // Tokens of sequence b: (pages - 1) * page_size + last page length (no pages: none).
+  std::vector<int64_t> tok((size_t)batch + 1, 0);
+  for (int b = 0; b < batch; ++b) {
+    const int64_t pages = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+    int64_t n = 0;
+    if (pages > 0) {
+      const int64_t last = page_size > 1 ? (int64_t)last_page_len[b] : 1;
+      if (last < 1 || last > page_size) return MLA_ERR_INDPTR;
+      n = (pages - 1) * page_size + last;
+      if (n > INT32_MAX) return MLA_ERR_INDPTR;  // token offsets inside a sequence are 32-bit
+    }
+    tok[(size_t)b + 1] = tok[(size_t)b] + n;
+  }
+  return plan_tokens(batch, tok, num_sms, opt, out);
 }
 
 }  // namespace mla

@@ -80,51 +80,54 @@ static_assert(Smem<MLA_MODE_FP8>::kBytes <= 232448, "fp8 stage-1 shared memory")
 
 __device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err, 0, code); }
 
-__device__ __forceinline__ bool item_has_tiles(const WorkItem& w, const int32_t* kv_indptr) {
-  return w.t_end > w.t_begin && (int64_t)kv_indptr[w.b + 1] - kv_indptr[w.b] == w.seq_len;
+__device__ __forceinline__ bool item_has_tiles(const WorkItem& w, const DecodeArgs& a) {
+  return w.t_end > w.t_begin && device_seq_tokens(a, w.b) == w.seq_len;
 }
 
 // Position in a CTA's stream of tiles.
 struct Cursor {
   int item, item_end;
-  int t, t_end;   // first row of the current tile / end row of the item (relative to the sequence)
-  int64_t base;   // kv_indices offset of the sequence's row 0
+  int t, t_end;   // first token of the current tile / end token of the item (relative to the sequence)
+  int64_t base;   // kv_indices offset of the sequence's first entry
 };
 
-__device__ __forceinline__ void cursor_settle(Cursor& c, const DevicePlan& p, const int32_t* kv_indptr) {
+__device__ __forceinline__ void cursor_settle(Cursor& c, const DevicePlan& p, const DecodeArgs& a) {
   while (c.item < c.item_end) {
     const WorkItem w = p.items[c.item];
-    if (item_has_tiles(w, kv_indptr)) {
+    if (item_has_tiles(w, a)) {
       c.t = w.t_begin;
       c.t_end = w.t_end;
-      c.base = kv_indptr[w.b];
+      c.base = a.kv_indptr[w.b];
       return;
     }
     ++c.item;
   }
 }
-__device__ __forceinline__ void cursor_next(Cursor& c, const DevicePlan& p, const int32_t* kv_indptr) {
+__device__ __forceinline__ void cursor_next(Cursor& c, const DevicePlan& p, const DecodeArgs& a) {
   if (c.item >= c.item_end) return;
   c.t += kTile;
   if (c.t >= c.t_end) {
     ++c.item;
-    cursor_settle(c, p, kv_indptr);
+    cursor_settle(c, p, a);
   }
 }
 
 // Source of one ring row of a future tile: state 0 = nothing, 1 = the zero
-// row (past the end of the item), 2 = KV row `idx`.
+// row (past the end of the item), 2 = token `t` of the sequence, whose
+// kv_indices entry (a row, or a page id) is `idx`.
 struct RowSrc {
   int state;
   int idx;
+  int t;
 };
 
-__device__ __forceinline__ RowSrc prefetch_row(const Cursor& c, int r, const int32_t* kv_indices) {
-  RowSrc s{0, 0};
+__device__ __forceinline__ RowSrc prefetch_row(const Cursor& c, int r, const DecodeArgs& a) {
+  RowSrc s{0, 0, 0};
   if (c.item >= c.item_end) return s;
   if (c.t + r < c.t_end) {
     s.state = 2;
-    s.idx = __ldg(kv_indices + c.base + c.t + r);
+    s.t = c.t + r;
+    s.idx = __ldg(a.kv_indices + c.base + token_entry(a, s.t));
   } else {
     s.state = 1;
   }
@@ -132,14 +135,15 @@ __device__ __forceinline__ RowSrc prefetch_row(const Cursor& c, int r, const int
 }
 
 template <int MODE>
-__device__ __forceinline__ void issue_row(const RowSrc& s, uint32_t dst, uint32_t bar, const uint8_t* kv,
+__device__ __forceinline__ void issue_row(const RowSrc& s, uint32_t dst, uint32_t bar, const DecodeArgs& a,
                                           const uint8_t* zero_row, int64_t num_kv_slots, int* err,
                                           uint64_t policy) {
   if (s.state == 0) return;
   const uint8_t* src = zero_row;
   if (s.state == 2) {
-    if (s.idx >= 0 && (num_kv_slots == 0 || s.idx < num_kv_slots))
-      src = kv + (int64_t)s.idx * Cfg<MODE>::kRowBytes;
+    const int64_t row = token_row(a, s.idx, s.t);
+    if (s.idx >= 0 && (num_kv_slots == 0 || row < num_kv_slots))
+      src = static_cast<const uint8_t*>(a.kv) + row * Cfg<MODE>::kRowBytes;
     else
       record_error(err, MLA_ERR_INDEX);
   }
@@ -213,10 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int n_tiles = 0;
   for (int it = item_begin; it < item_end; ++it) {
     const WorkItem w = p.items[it];
-    if (item_has_tiles(w, a.kv_indptr)) n_tiles += (w.t_end - w.t_begin + kTile - 1) / kTile;
+    if (item_has_tiles(w, a)) n_tiles += (w.t_end - w.t_begin + kTile - 1) / kTile;
   }
 
-  const uint8_t* kv = static_cast<const uint8_t*>(a.kv);
   const float kv_scale = (MODE == MLA_MODE_FP8) ? __ldg(a.kv_scale) : 1.0f;
   const float score_log2 = a.sm_scale * kv_scale * kLog2e;  // score -> base-2 exponent
   const uint64_t policy = ptx::l2_evict_first_policy();
@@ -226,23 +229,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool copier = lane < 8;
   const uint32_t my_dst = ring + my_row * C::kRowStride;
   Cursor pc{item_begin, item_end, 0, 0, 0};
-  cursor_settle(pc, p, a.kv_indptr);
+  cursor_settle(pc, p, a);
   const int n_pro = min(C::kStages - 1, n_tiles);
   if (tid == 0)
     for (int k = 0; k < n_pro; ++k) ptx::mbar_arrive_expect_tx(bar0 + 8u * k, kTile * C::kRowBytes);
   __syncthreads();  // barriers initialised, expected bytes registered before any copy lands
   for (int k = 0; k < n_pro; ++k) {
     if (copier) {
-      const RowSrc rs = prefetch_row(pc, my_row, a.kv_indices);
-      issue_row<MODE>(rs, my_dst + k * S::kStageBytes, bar0 + 8u * k, kv, zero_row, p.num_kv_slots, p.err, policy);
+      const RowSrc rs = prefetch_row(pc, my_row, a);
+      issue_row<MODE>(rs, my_dst + k * S::kStageBytes, bar0 + 8u * k, a, zero_row, p.num_kv_slots, p.err, policy);
     }
-    cursor_next(pc, p, a.kv_indptr);
+    cursor_next(pc, p, a);
   }
   // sources of tiles n_pro and n_pro + 1 (issued from the loop once stages free up)
-  RowSrc pf1 = copier ? prefetch_row(pc, my_row, a.kv_indices) : RowSrc{0, 0};
-  cursor_next(pc, p, a.kv_indptr);
-  RowSrc pf2 = copier ? prefetch_row(pc, my_row, a.kv_indices) : RowSrc{0, 0};
-  cursor_next(pc, p, a.kv_indptr);
+  RowSrc pf1 = copier ? prefetch_row(pc, my_row, a) : RowSrc{0, 0};
+  cursor_next(pc, p, a);
+  RowSrc pf2 = copier ? prefetch_row(pc, my_row, a) : RowSrc{0, 0};
+  cursor_next(pc, p, a);
 
   // ---- consumer state
   uint32_t qa[C::kQSteps][4];
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int it = item_begin; it < item_end; ++it) {
     const WorkItem w = p.items[it];
-    if ((int64_t)a.kv_indptr[w.b + 1] - a.kv_indptr[w.b] != w.seq_len) {
+    if (device_seq_tokens(a, w.b) != w.seq_len) {
       if (tid == 0) record_error(p.err, MLA_ERR_PLAN_MISMATCH);
       continue;  // skipped by the copy cursor as well
     }
@@ -324,11 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Barrier 1 also means every warp finished P.V of tile - 1: its stage is free.
       if (copier && ahead < n_tiles)
-        issue_row<MODE>(pf1, my_dst + next_stage * S::kStageBytes, bar0 + 8u * next_stage, kv, zero_row,
+        issue_row<MODE>(pf1, my_dst + next_stage * S::kStageBytes, bar0 + 8u * next_stage, a, zero_row,
                         p.num_kv_slots, p.err, policy);
       pf1 = pf2;
-      pf2 = copier ? prefetch_row(pc, my_row, a.kv_indices) : RowSrc{0, 0};
-      cursor_next(pc, p, a.kv_indptr);
+      pf2 = copier ? prefetch_row(pc, my_row, a) : RowSrc{0, 0};
+      cursor_next(pc, p, a);
 
       // ---------------- online softmax over the tile
       float tmax0 = red[g], tmax1 = red[g + 8];

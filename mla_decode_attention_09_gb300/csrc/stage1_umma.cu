@@ -21,8 +21,10 @@
 // scale 1 and the per-tensor kv_scale multiplies the scores and the output
 // (submission 690201 "V6c", custom_kernel).
 //
-// Warp roles (192 threads): warps 0-3 softmax and epilogue (warp w reads TMEM
-// lanes 32w..32w+31), warp 4 TMA producer and query staging, warp 5 TMEM
+// Warp roles (256 threads): warps 0-3 softmax and epilogue (warp w reads TMEM
+// lanes 32w..32w+31), warp 4 TMA producer and query staging, warps 6-7 extra
+// loaders for tiles copied row by row (one warp cannot issue those copies fast
+// enough to keep HBM busy; three can come close), warp 5 TMEM
 // allocation and the single MMA-issuing thread. The latent part of a tile
 // (512 B per row, needed until P.V finishes) lives in a 3-slot ring of 64 KB,
 // the rope part (64 B per row, needed only by the scores) in a 2-slot ring of
@@ -32,10 +34,13 @@
 // O in TMEM is rescaled only when a tile's max exceeds the reference by more
 // than 2^8, so P = 2^(s - m_ref) <= 256 stays inside e4m3's range.
 //
-// KV rows arrive by TMA: a tile whose 128 row indices are consecutive is five
-// 2-D box loads; any other tile uses 4-row gather loads. Rows past the end of
-// an item, and rows whose index is out of range, are read at an out-of-bounds
-// coordinate, which TMA fills with zeros.
+// A tile whose 128 rows are consecutive in the KV buffer arrives by TMA as
+// five 2-D box loads. Any other tile (rows scattered by kv_indices, or pages
+// shorter than a tile) is copied by the three loader warps with 16-byte
+// cp.async, one 512-byte latent row per instruction, into the same swizzled
+// layout the box loads produce. Rows past the end of an item, and rows whose index is out
+// of range, are read at an out-of-bounds coordinate (TMA) or zero-filled
+// (cp.async).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -60,7 +65,8 @@ constexpr int kQLat = 4 * 16 * 128;           // 8 KB: e4m3 query latent part, 4
 constexpr int kQBytes = kQLat + 16 * 64;      // + 1 KB rope part
 constexpr int kPBuf = kRowsU * 16;            // 2 KB: P^T [128 tokens][16 heads] e4m3
 constexpr uint32_t kTileTx = kLatStage + kRopeStage;
-constexpr int kThreadsU = 192;
+constexpr int kThreadsU = 256;
+constexpr int kLoaders = 3;                   // warps 4, 6, 7
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;                 // S^T: 2 buffers x 16 columns
 constexpr uint32_t kColO = 32;                // O^T: 2 buffers x 4 blocks x 16 columns
@@ -73,7 +79,7 @@ constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 16, 1, 1);
 constexpr uint32_t kLayoutSw64 = 4;
 
 enum : int {
-  kBFull = 0,     // [3] tile data landed (TMA tx)
+  kBFull = 0,     // [3] tile data landed (TMA tx, and every loader lane's cp.async arrival)
   kBLEmpty = 3,   // [3] latent slot free (P.V done)
   kBREmpty = 6,   // [2] rope slot free (scores done)
   kBSFull = 8,    // [2] S^T ready
@@ -105,8 +111,8 @@ static_assert(SU::kQ % 1024 == 0 && SU::kRope % 1024 == 0 && SU::kP % 16 == 0 &&
 
 __device__ __forceinline__ void record_error_u(int* err, int code) { atomicCAS(err, 0, code); }
 
-__device__ __forceinline__ bool has_tiles(const WorkItem& w, const int32_t* kv_indptr) {
-  return w.t_end > w.t_begin && (int64_t)kv_indptr[w.b + 1] - kv_indptr[w.b] == w.seq_len;
+__device__ __forceinline__ bool has_tiles(const WorkItem& w, const DecodeArgs& a) {
+  return w.t_end > w.t_begin && device_seq_tokens(a, w.b) == w.seq_len;
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -147,17 +153,17 @@ struct TCur {
   int k;          // index of the current item among the items that have tiles
   int t0, t_begin, t_end;
   int b;
-  int64_t base;   // kv_indices offset of the sequence's row 0
+  int64_t base;   // kv_indices offset of the sequence's first entry
   bool done;
 };
-__device__ __forceinline__ void tcur_settle(TCur& c, const DevicePlan& p, const int32_t* ip) {
+__device__ __forceinline__ void tcur_settle(TCur& c, const DevicePlan& p, const DecodeArgs& a) {
   while (c.it < c.it_end) {
     const WorkItem w = p.items[c.it];
-    if (has_tiles(w, ip)) {
+    if (has_tiles(w, a)) {
       c.t0 = c.t_begin = w.t_begin;
       c.t_end = w.t_end;
       c.b = w.b;
-      c.base = ip[w.b];
+      c.base = a.kv_indptr[w.b];
       c.done = false;
       return;
     }
@@ -165,27 +171,27 @@ __device__ __forceinline__ void tcur_settle(TCur& c, const DevicePlan& p, const 
   }
   c.done = true;
 }
-__device__ __forceinline__ void tcur_init(TCur& c, int it, int it_end, const DevicePlan& p, const int32_t* ip) {
+__device__ __forceinline__ void tcur_init(TCur& c, int it, int it_end, const DevicePlan& p, const DecodeArgs& a) {
   c.it = it;
   c.it_end = it_end;
   c.k = 0;
-  tcur_settle(c, p, ip);
+  tcur_settle(c, p, a);
 }
-__device__ __forceinline__ void tcur_next(TCur& c, const DevicePlan& p, const int32_t* ip) {
+__device__ __forceinline__ void tcur_next(TCur& c, const DevicePlan& p, const DecodeArgs& a) {
   if (c.done) return;
   c.t0 += kRowsU;
   if (c.t0 >= c.t_end) {
     ++c.it;
     ++c.k;
-    tcur_settle(c, p, ip);
+    tcur_settle(c, p, a);
   }
 }
 // Move to the first tile of the next item.
-__device__ __forceinline__ void tcur_next_item(TCur& c, const DevicePlan& p, const int32_t* ip) {
+__device__ __forceinline__ void tcur_next_item(TCur& c, const DevicePlan& p, const DecodeArgs& a) {
   if (c.done) return;
   ++c.it;
   ++c.k;
-  tcur_settle(c, p, ip);
+  tcur_settle(c, p, a);
 }
 
 // Warp-wide transpose reduction of 16 per-lane values: returns, in every lane,
@@ -224,7 +230,7 @@ __device__ __forceinline__ int q_offset(int h, int d0) {
 }
 
 struct KvMaps {
-  CUtensorMap lat_tile, lat_gather, rope_tile, rope_gather;
+  CUtensorMap lat_tile, rope_tile;
 };
 
 __global__ void __launch_bounds__(kThreadsU, 1)
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) {
-      ptx::mbar_init(bar(kBFull + i), 1);
+      ptx::mbar_init(bar(kBFull + i), 1 + 32 * kLoaders);  // producer lane 0 + one cp.async arrival per loader lane
       ptx::mbar_init(bar(kBLEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -281,33 +287,42 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const float kv_scale = __ldg(a.kv_scale);
   const float score_log2 = a.sm_scale * kv_scale * kLog2eU;
 
-  if (warp == 4) {
-    // ------------------------------------------------ producer: KV tiles + query staging
-    if (lane == 0) {
+  if (warp == 4 || warp >= 6) {
+    // ------------------------------------------------ loaders: KV tiles (+ query staging in warp 4)
+    // Every loader walks the same tile stream and takes the same box / row-copy
+    // decision from the same indices. Warp 4 issues the box loads and arrives for
+    // the other two loaders on such tiles, which they skip without waiting; the
+    // row copies of a scattered tile are split among the three loaders.
+    const bool main_loader = warp == 4;
+    const int g = main_loader ? 0 : warp - 5;  // loader rank 0..2
+    if (main_loader && lane == 0) {
       umma::tma_prefetch_desc(&tm.lat_tile);
-      umma::tma_prefetch_desc(&tm.lat_gather);
       umma::tma_prefetch_desc(&tm.rope_tile);
-      umma::tma_prefetch_desc(&tm.rope_gather);
     }
     const uint64_t pol = ptx::l2_evict_first_policy();
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    // row sources of one tile held by this lane: rows lane + 32 j. Index loads run two tiles
-    // ahead and are checked only when the tile is issued, so the loads stay in flight meanwhile.
+    // row sources of one tile held by this lane: tokens lane + 32 j. Index loads run two tiles
+    // ahead and are turned into rows and checked only when the tile is issued, so the loads
+    // stay in flight meanwhile.
     auto load_rows = [&](const TCur& t, int (&y)[4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = lane + 32 * j;
-        y[j] = (!t.done && r < t.t_end - t.t0) ? __ldg(a.kv_indices + t.base + t.t0 + r) : oob_row;
+        y[j] = (!t.done && r < t.t_end - t.t0) ? __ldg(a.kv_indices + t.base + token_entry(a, t.t0 + r)) : oob_row;
       }
     };
-    auto check_rows = [&](int nv, int (&y)[4]) {
+    // rows past the item, and rows outside [0, pool rows), read as zeros (out-of-bounds coordinate)
+    auto check_rows = [&](int t0, int nv, int (&y)[4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
+        const int64_t row = token_row(a, y[j], t0 + lane + 32 * j);
         if (lane + 32 * j >= nv) {
           y[j] = oob_row;
-        } else if (y[j] < 0 || (p.num_kv_slots > 0 && y[j] >= p.num_kv_slots)) {
+        } else if (y[j] < 0 || row >= oob_row) {
           record_error_u(p.err, MLA_ERR_INDEX);
           y[j] = oob_row;
+        } else {
+          y[j] = (int)row;
         }
       }
     };
@@ -337,70 +352,99 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // loads, so it runs only when no tile can be issued (the ring is full, or every
     // tile is issued); the first item's query lands while its first tiles are in flight.
     TCur c, c1, c2, qc;
-    tcur_init(c, item_begin, item_end, p, a.kv_indptr);
+    tcur_init(c, item_begin, item_end, p, a);
     c1 = c;
-    tcur_next(c1, p, a.kv_indptr);
+    tcur_next(c1, p, a);
     c2 = c1;
-    tcur_next(c2, p, a.kv_indptr);
+    tcur_next(c2, p, a);
     qc = c;
+    if (!main_loader) qc.done = true;
     int y0s[4], y1s[4];
     load_rows(c, y0s);
     load_rows(c1, y1s);
     bool q_loaded = false, q_advance = false;
     int i = 0;
     bool ok = true;
+    bool decided = false, cont = false;  // box / row-copy decision for tile c, taken once
+    int y0 = oob_row;
     IdleClock idle;
     while (!c.done || !qc.done) {
       bool progress = false, tile_blocked = c.done;
       if (!c.done) {
         const int ls = i % kLatStages, rs = i & 1;
-        bool ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
-        ready = ready && (i < kRopeStages || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
-        tile_blocked = !__shfl_sync(~0u, ready, 0);
-        if (!tile_blocked) {
+        const int nv = c.t_end - c.t0;
+        if (!decided) {
           // Box loads when the valid rows are consecutive. A tail tile may then
           // read rows past the item (other rows of the pool, or zeros past its
           // end): only done when the pool size is known, and the softmax zeroes
           // those value rows before P.V reads them.
-          const int nv = c.t_end - c.t0;
-          check_rows(nv, y0s);
-          const int y0 = __shfl_sync(~0u, y0s[0], 0);
-          bool cont = y0 != oob_row && (nv >= kRowsU || p.num_kv_slots > 0);
+          check_rows(c.t0, nv, y0s);
+          y0 = __shfl_sync(~0u, y0s[0], 0);
+          cont = y0 != oob_row && (nv >= kRowsU || p.num_kv_slots > 0);
 #pragma unroll
           for (int j = 0; j < 4; ++j) cont = cont && (lane + 32 * j >= nv || y0s[j] == y0 + lane + 32 * j);
           cont = __all_sync(~0u, cont);
+          decided = true;
+        }
+        bool ready = !main_loader && cont;  // nothing to copy or wait for
+        if (!ready) {
+          ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
+          ready = ready && (i < kRopeStages || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
+          ready = __shfl_sync(~0u, ready, 0);
+        }
+        tile_blocked = !ready;
+        if (ready) {
           const uint32_t fb = bar(kBFull + ls);
           const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
-          if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kTileTx);
-          __syncwarp();
           if (cont) {
-            if (lane < 4) umma::tma_load_2d(lat + lane * kBlk, &tm.lat_tile, lane * 128, y0, fb, pol);
-            if (lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
+            if (main_loader) {
+              if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kTileTx);
+              __syncwarp();
+              if (lane < 4) umma::tma_load_2d(lat + lane * kBlk, &tm.lat_tile, lane * 128, y0, fb, pol);
+              if (lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
+              if (lane == 0) umma::mbar_arrive_cnt(fb, 32 * (kLoaders - 1));  // for the loaders that skip it
+            }
           } else {
-            // lane g gathers rows 4g..4g+3; row r is held by lane (r & 31), slot (r >> 5)
-            int ys[4];
+            // Row r's index sits in lane (r & 31), slot (r >> 5); loader g copies the
+            // latent rows r = g mod 3 and the rope groups i = g mod 3. Latent: lane l
+            // copies 16-byte chunk l of the row's 512 bytes into column block l / 8 at
+            // chunk (l % 8) ^ (r % 8) (the 128-byte swizzle). Rope: 8 rows per
+            // instruction, lane l copies chunk l % 4 of row 8i + l / 4 at chunk
+            // (l % 4) ^ ((r / 2) % 4) (the 64-byte swizzle).
+            const uint8_t* kv8 = static_cast<const uint8_t*>(a.kv);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int src = (4 * lane + jj) & 31;
-              const int v0 = __shfl_sync(~0u, y0s[0], src), v1 = __shfl_sync(~0u, y0s[1], src);
-              const int v2 = __shfl_sync(~0u, y0s[2], src), v3 = __shfl_sync(~0u, y0s[3], src);
-              const int slot = lane >> 3;
-              ys[jj] = slot == 0 ? v0 : (slot == 1 ? v1 : (slot == 2 ? v2 : v3));
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll 2
+              for (int rr = (g + kLoaders - (32 * j) % kLoaders) % kLoaders; rr < 32; rr += kLoaders) {
+                const int r = 32 * j + rr;
+                const int yr = __shfl_sync(~0u, y0s[j], rr);
+                const bool valid = yr != oob_row;
+                const uint32_t dst = lat + (lane >> 3) * kBlk + r * 128 + ((((uint32_t)lane & 7u) ^ (r & 7)) << 4);
+                umma::cp_async_16(dst, kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 16 * lane, valid ? 16u : 0u, pol);
+              }
             }
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb)
-              umma::tma_gather4(lat + cb * kBlk + lane * 512, &tm.lat_gather, cb * 128, ys[0], ys[1], ys[2], ys[3], fb,
-                                pol);
-            umma::tma_gather4(rope + lane * 256, &tm.rope_gather, 512, ys[0], ys[1], ys[2], ys[3], fb, pol);
+            for (int i8 = 0; i8 < 16; ++i8) {
+              if (i8 % kLoaders != g) continue;
+              const int r = 8 * i8 + (lane >> 2);
+              const int yr = __shfl_sync(~0u, y0s[i8 >> 2], r & 31);
+              const bool valid = yr != oob_row;
+              const uint32_t dst = rope + r * 64 + ((((uint32_t)lane & 3u) ^ ((r >> 1) & 3)) << 4);
+              umma::cp_async_16(dst, kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 512 + 16 * (lane & 3),
+                                valid ? 16u : 0u, pol);
+            }
+            if (main_loader && lane == 0) umma::mbar_arrive(fb);
           }
+          if (main_loader || !cont) umma::cp_async_arrive_noinc(fb);
           // shift the index pipeline: tile i+1's indices are already loaded, request tile i+2's
 #pragma unroll
           for (int j = 0; j < 4; ++j) y0s[j] = y1s[j];
           load_rows(c2, y1s);
           c = c1;
           c1 = c2;
-          tcur_next(c2, p, a.kv_indptr);
+          tcur_next(c2, p, a);
           ++i;
+          decided = false;
           progress = true;
         }
       }
@@ -409,7 +453,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (!q_loaded) {
           if (tile_blocked) {
             if (q_advance) {
-              tcur_next_item(qc, p, a.kv_indptr);
+              tcur_next_item(qc, p, a);
               q_advance = false;
             }
             if (!qc.done) {
@@ -436,8 +480,9 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       }
     }
     if (!ok && lane == 0) record_error_u(p.err, MLA_ERR_TIMEOUT);
+    umma::cp_async_wait_all();
     // let issued loads land before the CTA can exit (they already have in the normal path)
-    for (int t = (i >= kLatStages ? i - kLatStages : 0); t < i; ++t) {
+    for (int t = (i >= kLatStages ? i - kLatStages : 0); main_loader && t < i; ++t) {
       const uint32_t b_ = bar(kBFull + t % kLatStages);
       const uint32_t par = (uint32_t)(t / kLatStages) & 1u;
       if (ptx::mbar_try_wait(b_, par)) continue;
@@ -455,6 +500,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
         const uint32_t d = tmem + kColS + 16u * (uint32_t)(i & 1);
         umma::fence_after_sync();
+        umma::fence_proxy_async_smem();  // cp.async (generic proxy) tile data before the tensor core reads it
 #pragma unroll
         for (int st = 0; st < 16; ++st) {
           const uint32_t kb = st >> 2, ko = (st & 3) * 32;
@@ -485,7 +531,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         umma::commit(bar(kBLEmpty + i % kLatStages));
       };
       TCur c, d;  // c: next scores tile, d: next P.V tile
-      tcur_init(c, item_begin, item_end, p, a.kv_indptr);
+      tcur_init(c, item_begin, item_end, p, a);
       d = c;
       int nq = 0, npv = 0;
       IdleClock idle;
@@ -497,7 +543,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           if (oready && ptx::mbar_test_wait(bar(kBPFull + (npv & 1)), (npv >> 1) & 1)) {
             issue_pv(d, npv);
             ++npv;
-            tcur_next(d, p, a.kv_indptr);
+            tcur_next(d, p, a);
             progress = true;
           }
         }
@@ -506,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           if (qready && ptx::mbar_test_wait(bar(kBFull + nq % kLatStages), (nq / kLatStages) & 1)) {
             issue_qk(c, nq);
             ++nq;
-            tcur_next(c, p, a.kv_indptr);
+            tcur_next(c, p, a);
             progress = true;
           }
         }
@@ -531,7 +577,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     bool aborted = false;
     for (int it = item_begin; it < item_end && !aborted; ++it) {
       const WorkItem w = p.items[it];
-      if ((int64_t)a.kv_indptr[w.b + 1] - a.kv_indptr[w.b] != w.seq_len) {
+      if (device_seq_tokens(a, w.b) != w.seq_len) {
         if (tid == 0) record_error_u(p.err, MLA_ERR_PLAN_MISMATCH);
         continue;
       }
@@ -706,9 +752,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Four views of the e4m3 KV pool [rows x 576 bytes]: latent part in 128-byte
-// boxes (128-byte swizzle) and rope part in 64-byte boxes (64-byte swizzle),
-// each as 128-row tiles and as single rows for 4-row gathers.
+// Two views of the e4m3 KV pool [rows x 576 bytes] as 128-row tiles: the
+// latent part in 128-byte boxes (128-byte swizzle) and the rope part in
+// 64-byte boxes (64-byte swizzle).
 int make_kv_maps(const void* kv, int64_t rows, KvMaps* m) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
@@ -721,10 +767,8 @@ int make_kv_maps(const void* kv, int64_t rows, KvMaps* m) {
     cuuint32_t w, h;
     CUtensorMapSwizzle sw;
   };
-  const View views[4] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
-                         {&m->lat_gather, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B},
-                         {&m->rope_tile, 64, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_64B},
-                         {&m->rope_gather, 64, 1, CU_TENSOR_MAP_SWIZZLE_64B}};
+  const View views[2] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
+                         {&m->rope_tile, 64, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_64B}};
   for (const View& v : views) {
     const cuuint32_t box[2] = {v.w, v.h};
     if (enc(v.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, v.sw,

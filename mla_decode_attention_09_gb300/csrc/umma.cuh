@@ -1,7 +1,7 @@
 // Inline-PTX wrappers for the 5th-generation tensor core path of sm_103a:
 // TMEM allocation, tcgen05.mma (kind::f8f6f4) with shared-memory matrix
-// descriptors, tcgen05.commit to mbarriers, TMEM loads/stores, and TMA tensor
-// loads (tiled and 4-row gather).
+// descriptors, tcgen05.commit to mbarriers, TMEM loads/stores, TMA tensor
+// loads (tiled and 4-row gather) and 16-byte cp.async row copies.
 #pragma once
 
 #include <cuda.h>
@@ -122,6 +122,20 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned). With
+// src_bytes = 0 nothing is read and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
+}
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed; the barrier's expected arrival count includes this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads (tensor core, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -129,6 +143,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.release.cta.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar)
+               : "memory");
+}
+// `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.release.cta.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
+               "r"(count)
                : "memory");
 }
 

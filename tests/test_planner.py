@@ -108,3 +108,50 @@ def test_plan_rejects_bad_indptr():
     with pytest.raises(mla.MLAError) as e:
         mla.plan_compute_host(np.array([0, 5], dtype=np.int32), 0)
     assert e.value.status == -1
+
+
+# ---------------------------------------------------------------- paged layout
+
+def _paged_layout(lengths, ps):
+    pages = [(L + ps - 1) // ps for L in lengths]
+    ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+    ip[1:] = np.cumsum(pages)
+    last = np.array([L - (p - 1) * ps if p else 1 for L, p in zip(lengths, pages)], dtype=np.int32)
+    return ip, last
+
+
+@pytest.mark.parametrize("ps", [1, 2, 3, 8, 64, 300])
+def test_paged_plan_equals_row_plan_on_token_counts(ps):
+    """A paged plan is the row plan of the sequences' token counts: (pages - 1) * page_size + last."""
+    lengths = [0, 1, 17, 1000, 5, 8192, 129, 300, 301]
+    ip, last = _paged_layout(lengths, ps)
+    opts = dict(min_rows_per_split=16, granularity=16)
+    got = mla.plan_compute_host_paged(ip, last, ps, 11, **opts)
+    tok = np.zeros(len(lengths) + 1, dtype=np.int32)
+    tok[1:] = np.cumsum(lengths)
+    ref = mla.plan_compute_host(tok, 11, **opts)
+    for k in ("items", "work_indptr", "reduce"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert got["num_slots"] == ref["num_slots"]
+    assert [int(L) for L in got["items"][:, 4]] == [lengths[b] for b in got["items"][:, 0]]
+
+
+def test_paged_plan_rejects_bad_layouts():
+    ip = np.array([0, 2, 3], dtype=np.int32)
+    for bad in ([0, 1], [1, 9], [-1, 1]):
+        with pytest.raises(mla.MLAError) as e:
+            mla.plan_compute_host_paged(ip, np.array(bad, dtype=np.int32), 8, 4)
+        assert e.value.status == -10
+    # no pages: the last page length is not looked at
+    r = mla.plan_compute_host_paged(np.array([0, 0, 1], dtype=np.int32), np.array([0, 3], dtype=np.int32), 8, 4)
+    assert [int(x) for x in r["items"][:, 4]] == [0, 3]
+    with pytest.raises(mla.MLAError) as e:
+        mla.plan_compute_host_paged(ip, np.array([1, 1], dtype=np.int32), 0, 4)
+    assert e.value.status == -1
+    with pytest.raises(mla.MLAError) as e:
+        mla.plan_compute_host_paged(ip, None, 8, 4)
+    assert e.value.status == -1
+    # a sequence of more than 2^31 - 1 tokens does not fit the 32-bit token offsets
+    with pytest.raises(mla.MLAError) as e:
+        mla.plan_compute_host_paged(np.array([0, 1 << 24], dtype=np.int32), np.array([256], dtype=np.int32), 256, 4)
+    assert e.value.status == -10
