@@ -98,24 +98,31 @@ struct DecodeArgs {
 };
 
 #ifdef __CUDACC__
+// Token addressing, specialised at compile time: kPaged = false is the row
+// layout (every kv_indices entry is a row, lengths are kv_indptr differences);
+// kPaged = true takes pages of a.page_size tokens.
+//
 // Tokens of sequence b according to the device arrays: pages of page_size
 // tokens, the last one holding kv_last_page_len[b]. -1 when that length lies
 // outside [1, page_size] (the caller treats it like a plan mismatch).
+template <bool kPaged>
 __device__ __forceinline__ int64_t device_seq_tokens(const DecodeArgs& a, int b) {
   const int64_t pages = (int64_t)a.kv_indptr[b + 1] - a.kv_indptr[b];
-  if (a.page_size <= 1 || pages <= 0) return pages;
+  if (!kPaged || pages <= 0) return pages;
   const int last = a.kv_last_page_len[b];
   if (last < 1 || last > a.page_size) return -1;
   return (pages - 1) * a.page_size + last;
 }
 // kv_indices position (relative to the sequence's first entry) of token t.
+template <bool kPaged>
 __device__ __forceinline__ int token_entry(const DecodeArgs& a, int t) {
-  return a.page_size <= 1 ? t : t / a.page_size;
+  return kPaged ? t / a.page_size : t;
 }
 // KV row of token t given the kv_indices entry e that token_entry pointed at
 // (entry * page_size + t % page_size), in 64 bits: a caller range-checks it.
+template <bool kPaged>
 __device__ __forceinline__ int64_t token_row(const DecodeArgs& a, int32_t e, int t) {
-  return a.page_size <= 1 ? (int64_t)e : (int64_t)e * a.page_size + t % a.page_size;
+  return kPaged ? (int64_t)e * a.page_size + t % a.page_size : (int64_t)e;
 }
 #endif
 

@@ -80,8 +80,9 @@ static_assert(Smem<MLA_MODE_FP8>::kBytes <= 232448, "fp8 stage-1 shared memory")
 
 __device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err, 0, code); }
 
+template <bool kPaged>
 __device__ __forceinline__ bool item_has_tiles(const WorkItem& w, const DecodeArgs& a) {
-  return w.t_end > w.t_begin && device_seq_tokens(a, w.b) == w.seq_len;
+  return w.t_end > w.t_begin && device_seq_tokens<kPaged>(a, w.b) == w.seq_len;
 }
 
 // Position in a CTA's stream of tiles.
@@ -91,10 +92,11 @@ struct Cursor {
   int64_t base;   // kv_indices offset of the sequence's first entry
 };
 
+template <bool kPaged>
 __device__ __forceinline__ void cursor_settle(Cursor& c, const DevicePlan& p, const DecodeArgs& a) {
   while (c.item < c.item_end) {
     const WorkItem w = p.items[c.item];
-    if (item_has_tiles(w, a)) {
+    if (item_has_tiles<kPaged>(w, a)) {
       c.t = w.t_begin;
       c.t_end = w.t_end;
       c.base = a.kv_indptr[w.b];
@@ -103,12 +105,13 @@ __device__ __forceinline__ void cursor_settle(Cursor& c, const DevicePlan& p, co
     ++c.item;
   }
 }
+template <bool kPaged>
 __device__ __forceinline__ void cursor_next(Cursor& c, const DevicePlan& p, const DecodeArgs& a) {
   if (c.item >= c.item_end) return;
   c.t += kTile;
   if (c.t >= c.t_end) {
     ++c.item;
-    cursor_settle(c, p, a);
+    cursor_settle<kPaged>(c, p, a);
   }
 }
 
@@ -121,27 +124,28 @@ struct RowSrc {
   int t;
 };
 
+template <bool kPaged>
 __device__ __forceinline__ RowSrc prefetch_row(const Cursor& c, int r, const DecodeArgs& a) {
   RowSrc s{0, 0, 0};
   if (c.item >= c.item_end) return s;
   if (c.t + r < c.t_end) {
     s.state = 2;
     s.t = c.t + r;
-    s.idx = __ldg(a.kv_indices + c.base + token_entry(a, s.t));
+    s.idx = __ldg(a.kv_indices + c.base + token_entry<kPaged>(a, s.t));
   } else {
     s.state = 1;
   }
   return s;
 }
 
-template <int MODE>
+template <int MODE, bool kPaged>
 __device__ __forceinline__ void issue_row(const RowSrc& s, uint32_t dst, uint32_t bar, const DecodeArgs& a,
                                           const uint8_t* zero_row, int64_t num_kv_slots, int* err,
                                           uint64_t policy) {
   if (s.state == 0) return;
   const uint8_t* src = zero_row;
   if (s.state == 2) {
-    const int64_t row = token_row(a, s.idx, s.t);
+    const int64_t row = token_row<kPaged>(a, s.idx, s.t);
     if (s.idx >= 0 && (num_kv_slots == 0 || row < num_kv_slots))
       src = static_cast<const uint8_t*>(a.kv) + row * Cfg<MODE>::kRowBytes;
     else
@@ -185,7 +189,7 @@ __device__ __forceinline__ void load_q(uint32_t (&qa)[Cfg<MODE>::kQSteps][4], co
   }
 }
 
-template <int MODE>
+template <int MODE, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_stage1_kernel(const DecodeArgs a, const DevicePlan p, const uint8_t* __restrict__ zero_row) {
   using C = Cfg<MODE>;
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int n_tiles = 0;
   for (int it = item_begin; it < item_end; ++it) {
     const WorkItem w = p.items[it];
-    if (item_has_tiles(w, a)) n_tiles += (w.t_end - w.t_begin + kTile - 1) / kTile;
+    if (item_has_tiles<kPaged>(w, a)) n_tiles += (w.t_end - w.t_begin + kTile - 1) / kTile;
   }
 
   const float kv_scale = (MODE == MLA_MODE_FP8) ? __ldg(a.kv_scale) : 1.0f;
@@ -229,23 +233,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool copier = lane < 8;
   const uint32_t my_dst = ring + my_row * C::kRowStride;
   Cursor pc{item_begin, item_end, 0, 0, 0};
-  cursor_settle(pc, p, a);
+  cursor_settle<kPaged>(pc, p, a);
   const int n_pro = min(C::kStages - 1, n_tiles);
   if (tid == 0)
     for (int k = 0; k < n_pro; ++k) ptx::mbar_arrive_expect_tx(bar0 + 8u * k, kTile * C::kRowBytes);
   __syncthreads();  // barriers initialised, expected bytes registered before any copy lands
   for (int k = 0; k < n_pro; ++k) {
     if (copier) {
-      const RowSrc rs = prefetch_row(pc, my_row, a);
-      issue_row<MODE>(rs, my_dst + k * S::kStageBytes, bar0 + 8u * k, a, zero_row, p.num_kv_slots, p.err, policy);
+      const RowSrc rs = prefetch_row<kPaged>(pc, my_row, a);
+      issue_row<MODE, kPaged>(rs, my_dst + k * S::kStageBytes, bar0 + 8u * k, a, zero_row, p.num_kv_slots, p.err, policy);
     }
-    cursor_next(pc, p, a);
+    cursor_next<kPaged>(pc, p, a);
   }
   // sources of tiles n_pro and n_pro + 1 (issued from the loop once stages free up)
-  RowSrc pf1 = copier ? prefetch_row(pc, my_row, a) : RowSrc{0, 0};
-  cursor_next(pc, p, a);
-  RowSrc pf2 = copier ? prefetch_row(pc, my_row, a) : RowSrc{0, 0};
-  cursor_next(pc, p, a);
+  RowSrc pf1 = copier ? prefetch_row<kPaged>(pc, my_row, a) : RowSrc{0, 0};
+  cursor_next<kPaged>(pc, p, a);
+  RowSrc pf2 = copier ? prefetch_row<kPaged>(pc, my_row, a) : RowSrc{0, 0};
+  cursor_next<kPaged>(pc, p, a);
 
   // ---- consumer state
   uint32_t qa[C::kQSteps][4];
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int it = item_begin; it < item_end; ++it) {
     const WorkItem w = p.items[it];
-    if (device_seq_tokens(a, w.b) != w.seq_len) {
+    if (device_seq_tokens<kPaged>(a, w.b) != w.seq_len) {
       if (tid == 0) record_error(p.err, MLA_ERR_PLAN_MISMATCH);
       continue;  // skipped by the copy cursor as well
     }
@@ -327,11 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Barrier 1 also means every warp finished P.V of tile - 1: its stage is free.
       if (copier && ahead < n_tiles)
-        issue_row<MODE>(pf1, my_dst + next_stage * S::kStageBytes, bar0 + 8u * next_stage, a, zero_row,
+        issue_row<MODE, kPaged>(pf1, my_dst + next_stage * S::kStageBytes, bar0 + 8u * next_stage, a, zero_row,
                         p.num_kv_slots, p.err, policy);
       pf1 = pf2;
-      pf2 = copier ? prefetch_row(pc, my_row, a) : RowSrc{0, 0};
-      cursor_next(pc, p, a);
+      pf2 = copier ? prefetch_row<kPaged>(pc, my_row, a) : RowSrc{0, 0};
+      cursor_next<kPaged>(pc, p, a);
 
       // ---------------- online softmax over the tile
       float tmax0 = red[g], tmax1 = red[g + 8];
@@ -512,15 +516,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE>
-int launch_stage1_t(const DecodeArgs& a, const DevicePlan& p, const uint8_t* zero_row, cudaStream_t stream) {
-  static bool configured[64] = {};  // the shared-memory opt-in is set once per device
+template <int MODE, bool kPaged>
+int launch_stage1_tp(const DecodeArgs& a, const DevicePlan& p, const uint8_t* zero_row, cudaStream_t stream) {
+  static bool configured[64] = {};  // the shared-memory opt-in is set once per device and instance
   const int smem_bytes = Smem<MODE>::kBytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(mla_stage1_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    e = cudaFuncSetAttribute(mla_stage1_kernel<MODE, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return (int)e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
@@ -536,7 +540,13 @@ int launch_stage1_t(const DecodeArgs& a, const DevicePlan& p, const uint8_t* zer
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_kernel<MODE>, a, p, zero_row);
+  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_kernel<MODE, kPaged>, a, p, zero_row);
+}
+
+template <int MODE>
+int launch_stage1_t(const DecodeArgs& a, const DevicePlan& p, const uint8_t* zero_row, cudaStream_t stream) {
+  return a.page_size > 1 ? launch_stage1_tp<MODE, true>(a, p, zero_row, stream)
+                         : launch_stage1_tp<MODE, false>(a, p, zero_row, stream);
 }
 
 }  // namespace

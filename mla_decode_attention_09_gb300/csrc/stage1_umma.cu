@@ -102,7 +102,8 @@ struct SU {
   static constexpr int kBar = kLsum + 64 * 4;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kBytes = kAbort + 4;
+  static constexpr int kRowCopy = kAbort + 4;                   // [3] latent slot holds a row-copied tile
+  static constexpr int kBytes = kRowCopy + 3 * 4;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 inside the kernel
 };
 static_assert(SU::kAlloc <= 232448, "tcgen05 stage-1 shared memory");
@@ -111,8 +112,9 @@ static_assert(SU::kQ % 1024 == 0 && SU::kRope % 1024 == 0 && SU::kP % 16 == 0 &&
 
 __device__ __forceinline__ void record_error_u(int* err, int code) { atomicCAS(err, 0, code); }
 
+template <bool kPaged>
 __device__ __forceinline__ bool has_tiles(const WorkItem& w, const DecodeArgs& a) {
-  return w.t_end > w.t_begin && device_seq_tokens(a, w.b) == w.seq_len;
+  return w.t_end > w.t_begin && device_seq_tokens<kPaged>(a, w.b) == w.seq_len;
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -156,10 +158,11 @@ struct TCur {
   int64_t base;   // kv_indices offset of the sequence's first entry
   bool done;
 };
+template <bool kPaged>
 __device__ __forceinline__ void tcur_settle(TCur& c, const DevicePlan& p, const DecodeArgs& a) {
   while (c.it < c.it_end) {
     const WorkItem w = p.items[c.it];
-    if (has_tiles(w, a)) {
+    if (has_tiles<kPaged>(w, a)) {
       c.t0 = c.t_begin = w.t_begin;
       c.t_end = w.t_end;
       c.b = w.b;
@@ -171,27 +174,30 @@ __device__ __forceinline__ void tcur_settle(TCur& c, const DevicePlan& p, const 
   }
   c.done = true;
 }
+template <bool kPaged>
 __device__ __forceinline__ void tcur_init(TCur& c, int it, int it_end, const DevicePlan& p, const DecodeArgs& a) {
   c.it = it;
   c.it_end = it_end;
   c.k = 0;
-  tcur_settle(c, p, a);
+  tcur_settle<kPaged>(c, p, a);
 }
+template <bool kPaged>
 __device__ __forceinline__ void tcur_next(TCur& c, const DevicePlan& p, const DecodeArgs& a) {
   if (c.done) return;
   c.t0 += kRowsU;
   if (c.t0 >= c.t_end) {
     ++c.it;
     ++c.k;
-    tcur_settle(c, p, a);
+    tcur_settle<kPaged>(c, p, a);
   }
 }
 // Move to the first tile of the next item.
+template <bool kPaged>
 __device__ __forceinline__ void tcur_next_item(TCur& c, const DevicePlan& p, const DecodeArgs& a) {
   if (c.done) return;
   ++c.it;
   ++c.k;
-  tcur_settle(c, p, a);
+  tcur_settle<kPaged>(c, p, a);
 }
 
 // Warp-wide transpose reduction of 16 per-lane values: returns, in every lane,
@@ -233,6 +239,7 @@ struct KvMaps {
   CUtensorMap lat_tile, rope_tile;
 };
 
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreadsU, 1)
     mla_stage1_fp8_umma_kernel(const DecodeArgs a, const DevicePlan p, const __grid_constant__ KvMaps tm,
                                const int32_t oob_row) {
@@ -249,6 +256,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   float* red = reinterpret_cast<float*>(smem + SU::kRed);
   float* lsum = reinterpret_cast<float*>(smem + SU::kLsum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SU::kAbort);
+  volatile int* row_copy = reinterpret_cast<volatile int*>(smem + SU::kRowCopy);
   auto bar = [&](int i) { return base + SU::kBar + 8u * (uint32_t)i; };
 
   if (tid == 0) {
@@ -308,14 +316,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = lane + 32 * j;
-        y[j] = (!t.done && r < t.t_end - t.t0) ? __ldg(a.kv_indices + t.base + token_entry(a, t.t0 + r)) : oob_row;
+        y[j] = (!t.done && r < t.t_end - t.t0) ? __ldg(a.kv_indices + t.base + token_entry<kPaged>(a, t.t0 + r)) : oob_row;
       }
     };
     // rows past the item, and rows outside [0, pool rows), read as zeros (out-of-bounds coordinate)
     auto check_rows = [&](int t0, int nv, int (&y)[4]) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int64_t row = token_row(a, y[j], t0 + lane + 32 * j);
+        const int64_t row = token_row<kPaged>(a, y[j], t0 + lane + 32 * j);
         if (lane + 32 * j >= nv) {
           y[j] = oob_row;
         } else if (y[j] < 0 || row >= oob_row) {
@@ -352,11 +360,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // loads, so it runs only when no tile can be issued (the ring is full, or every
     // tile is issued); the first item's query lands while its first tiles are in flight.
     TCur c, c1, c2, qc;
-    tcur_init(c, item_begin, item_end, p, a);
+    tcur_init<kPaged>(c, item_begin, item_end, p, a);
     c1 = c;
-    tcur_next(c1, p, a);
+    tcur_next<kPaged>(c1, p, a);
     c2 = c1;
-    tcur_next(c2, p, a);
+    tcur_next<kPaged>(c2, p, a);
     qc = c;
     if (!main_loader) qc.done = true;
     int y0s[4], y1s[4];
@@ -396,6 +404,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (ready) {
           const uint32_t fb = bar(kBFull + ls);
           const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
+          if (main_loader && lane == 0) row_copy[ls] = cont ? 0 : 1;  // published by the arrivals below
           if (cont) {
             if (main_loader) {
               if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kTileTx);
@@ -442,7 +451,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           load_rows(c2, y1s);
           c = c1;
           c1 = c2;
-          tcur_next(c2, p, a);
+          tcur_next<kPaged>(c2, p, a);
           ++i;
           decided = false;
           progress = true;
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (!q_loaded) {
           if (tile_blocked) {
             if (q_advance) {
-              tcur_next_item(qc, p, a);
+              tcur_next_item<kPaged>(qc, p, a);
               q_advance = false;
             }
             if (!qc.done) {
@@ -500,7 +509,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
         const uint32_t d = tmem + kColS + 16u * (uint32_t)(i & 1);
         umma::fence_after_sync();
-        umma::fence_proxy_async_smem();  // cp.async (generic proxy) tile data before the tensor core reads it
+        // row-copied tile: order the cp.async (generic proxy) writes before the tensor core reads them
+        if (row_copy[i % kLatStages]) umma::fence_proxy_async_smem();
 #pragma unroll
         for (int st = 0; st < 16; ++st) {
           const uint32_t kb = st >> 2, ko = (st & 3) * 32;
@@ -531,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         umma::commit(bar(kBLEmpty + i % kLatStages));
       };
       TCur c, d;  // c: next scores tile, d: next P.V tile
-      tcur_init(c, item_begin, item_end, p, a);
+      tcur_init<kPaged>(c, item_begin, item_end, p, a);
       d = c;
       int nq = 0, npv = 0;
       IdleClock idle;
@@ -543,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           if (oready && ptx::mbar_test_wait(bar(kBPFull + (npv & 1)), (npv >> 1) & 1)) {
             issue_pv(d, npv);
             ++npv;
-            tcur_next(d, p, a);
+            tcur_next<kPaged>(d, p, a);
             progress = true;
           }
         }
@@ -552,7 +562,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           if (qready && ptx::mbar_test_wait(bar(kBFull + nq % kLatStages), (nq / kLatStages) & 1)) {
             issue_qk(c, nq);
             ++nq;
-            tcur_next(c, p, a);
+            tcur_next<kPaged>(c, p, a);
             progress = true;
           }
         }
@@ -577,7 +587,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     bool aborted = false;
     for (int it = item_begin; it < item_end && !aborted; ++it) {
       const WorkItem w = p.items[it];
-      if (device_seq_tokens(a, w.b) != w.seq_len) {
+      if (device_seq_tokens<kPaged>(a, w.b) != w.seq_len) {
         if (tid == 0) record_error_u(p.err, MLA_ERR_PLAN_MISMATCH);
         continue;
       }
@@ -786,7 +796,11 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(mla_stage1_fp8_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SU::kAlloc);
+    e = cudaFuncSetAttribute(mla_stage1_fp8_umma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SU::kAlloc);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_stage1_fp8_umma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SU::kAlloc);
     if (e != cudaSuccess) return (int)e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
@@ -812,7 +826,8 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel, a, p, maps, (int32_t)rows);
+  if (a.page_size > 1) return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<true>, a, p, maps, (int32_t)rows);
+  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<false>, a, p, maps, (int32_t)rows);
 }
 
 }  // namespace mla
