@@ -228,7 +228,7 @@ def bench_ours(args):
     init_dist(ws, "nccl")
     dev = torch.device("cuda", local)
     mla_build.build()
-    w = mi.WORKLOADS[args.workload]
+    w = mi.get_workload(args.workload)
     nbytes = mi.workload_bytes(w)
     step_bytes = nbytes["total"]
 
@@ -339,7 +339,7 @@ def bench_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "us_per_call": round(ms_per_step * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if w.mode == mi.MODE_FP8 else "bf16", "data": "synthetic",
+        "dtype": {mi.MODE_BF16: "bf16", mi.MODE_FP8: "e4m3", mi.MODE_A16W8: "f16"}[w.mode], "data": "synthetic",
         "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
                    "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": 1, "bytes_per_call": step_bytes,
                    "l2": "inputs larger than L2, two copies alternate", "timing": "CUDA graphs of decode calls",
@@ -440,7 +440,7 @@ def bench_reference(args):
     if rank != 0:
         return
     import oracle
-    w = mi.WORKLOADS[args.workload]
+    w = mi.get_workload(args.workload)
     host = mi.make_workload(w)
     lib = oracle.load()
     lens = host.lengths()
@@ -483,7 +483,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="fp8_b64_l8192", choices=list(mi.WORKLOADS))
+    ap.add_argument("--workload", default="fp8_b64_l8192", choices=list(mi.WORKLOADS) + list(mi.EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--all-workloads", action="store_true", help="add µs/call of every workload to the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -54,7 +54,14 @@ enum mla_dtype_mode {
      per-tensor dequantisation scale *kv_scale (kv_data["fp8"] = (buffer,
      scale)). Scores use q8 . k8 * sm_scale * kv_scale; out is scaled by
      kv_scale. */
-  MLA_MODE_FP8 = 1
+  MLA_MODE_FP8 = 1,
+  /* "a16w8" (submission 598454 "v12", docstring: activations in their original
+     precision, KV in fp8): q bf16 [B,16,576] used at bf16 precision (converted
+     to f16 inside the kernel: exact for 2^-14 <= |q| < 65520, saturating at
+     65504 beyond), kv e4m3fn bytes [slots,576] with *kv_scale as in
+     MLA_MODE_FP8. Runs on the warp-level kernel (the 5th-generation tensor
+     cores take no bf16 x e4m3 product). */
+  MLA_MODE_A16W8 = 2
 };
 
 /* Status codes. */
@@ -138,7 +145,7 @@ int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info);
  * mla_decode — one decode call: stage 1 (+ reduce when any sequence is split).
  *   q          device bf16 [B,16,576], row-major, 16-byte aligned.
  *   kv         device [num_slots,576] row-major: bf16 (MLA_MODE_BF16) or e4m3fn
- *              bytes (MLA_MODE_FP8); 16-byte aligned.
+ *              bytes (MLA_MODE_FP8, MLA_MODE_A16W8); 16-byte aligned.
  *   kv_scale   device fp32 [1]: fp8 dequantisation scale (ignored in bf16 mode,
  *              may then be NULL).
  *   kv_indptr  device int32 [B+1], equal to the host array the plan was built

@@ -25,6 +25,7 @@ V_DIM = 512
 SM_SCALE = 1.0 / math.sqrt(QK_DIM)
 MODE_BF16 = 0
 MODE_FP8 = 1
+MODE_A16W8 = 2  # bf16 q x e4m3 kv (pass dtype_mode explicitly: kv bytes alone do not tell it from MODE_FP8)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmla_decode.so")
@@ -223,8 +224,8 @@ def _validate(q, kv, kv_scale, kv_indptr, kv_indices, out, mode, p: Plan):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if kv_indptr.dtype != torch.int32 or kv_indices.dtype != torch.int32:
         raise ValueError("kv_indptr and kv_indices must be int32")
-    if mode == MODE_FP8 and (kv_scale is None or kv_scale.dtype != torch.float32 or not kv_scale.is_cuda):
-        raise ValueError("fp8 mode needs kv_scale as a float32 CUDA tensor of one element")
+    if mode != MODE_BF16 and (kv_scale is None or kv_scale.dtype != torch.float32 or not kv_scale.is_cuda):
+        raise ValueError("fp8 KV needs kv_scale as a float32 CUDA tensor of one element")
 
 
 def _call(fn, q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale, mode, p, stream):

@@ -155,11 +155,12 @@ int validate_decode(const void* q, const void* kv, const float* kv_scale, const 
   if (!plan || plan->refcount <= 0) return MLA_ERR_ARG;
   if (plan->paged != l.paged || plan->page_size != l.page_size) return MLA_ERR_ARG;
   if (l.paged && l.page_size > 1 && plan->batch > 0 && !l.last) return MLA_ERR_ARG;
-  if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8) return MLA_ERR_DTYPE;
+  if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8 && dtype_mode != MLA_MODE_A16W8)
+    return MLA_ERR_DTYPE;
   if (plan->batch > 0) {
     if (!q || !kv || !kv_indptr || !out) return MLA_ERR_ARG;
     if (plan->host.total_rows > 0 && !kv_indices) return MLA_ERR_ARG;
-    if (dtype_mode == MLA_MODE_FP8 && !kv_scale) return MLA_ERR_ARG;
+    if (dtype_mode != MLA_MODE_BF16 && !kv_scale) return MLA_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(out)) & 15)
       return MLA_ERR_ALIGN;
   }

@@ -169,11 +169,12 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const float* kv
                                   const int32_t* kv_indices, int batch, int64_t num_kv_slots, void* out,
                                   float sm_scale, int dtype_mode, int* status_dev, void* stream) {
   using namespace mla;
-  if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8) return MLA_ERR_DTYPE;
+  if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8 && dtype_mode != MLA_MODE_A16W8)
+    return MLA_ERR_DTYPE;
   if (batch < 0 || !status_dev || (batch > 0 && (!kv_indptr_host || !q || !kv || !kv_indptr || !out)))
     return MLA_ERR_ARG;
   if (batch > kMaxBatch) return MLA_ERR_NOALLOC_LIMIT;
-  if (dtype_mode == MLA_MODE_FP8 && batch > 0 && !kv_scale) return MLA_ERR_ARG;
+  if (dtype_mode != MLA_MODE_BF16 && batch > 0 && !kv_scale) return MLA_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(out)) & 15)
     return MLA_ERR_ALIGN;
   int dev = -1;

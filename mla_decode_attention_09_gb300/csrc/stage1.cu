@@ -27,6 +27,17 @@
 // assembled from 32-bit shared loads with byte permutes; mma-k is mapped to
 // tile rows as k = 16h + 4c + j -> row 16h + 2c + (j & 1) + 8 (j >> 1), which
 // keeps those loads free of bank conflicts, and P is stored in that k order.
+//
+// a16w8 mode (bf16 Q x e4m3 KV, the "a16w8" configuration of kernelbot
+// amd-mixed-mla submission 598454 "v12", docstring): f16 m16n8k16 mma. Q is
+// converted bf16 -> f16 once per item (exact for 2^-14 <= |q| < 65520,
+// saturating beyond), every e4m3 key and value byte converts to f16 exactly,
+// and P is f16. Keys keep the e4m3 ring layout: the four bytes one lane gets
+// from an 8-row ldmatrix (dims 4c..4c+3 of a 16-dim chunk) become that lane's
+// two B registers, so mma-k 2c, 2c+1 <- dims 4c, 4c+1 and mma-k 2c+8, 2c+9 <-
+// dims 4c+2, 4c+3, and the Q fragments follow the same order. Values reuse the
+// e4m3 V fragments: their four bytes are rows 2c, 2c+1, 2c+8, 2c+9 of a
+// 16-row half, which is the natural m16n8k16 k order, so P stays in row order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -64,6 +75,14 @@ struct Cfg<MLA_MODE_FP8> {
   static constexpr int kPStride = kTile + 16;        // e4m3 P row of one head (80 B)
   static constexpr int kQSteps = kQkDim / 32;        // 18
 };
+template <>
+struct Cfg<MLA_MODE_A16W8> {
+  static constexpr int kRowBytes = kQkDim;           // 576: e4m3 rows
+  static constexpr int kRowStride = kRowBytes + 16;  // 592
+  static constexpr int kStages = 5;
+  static constexpr int kPStride = kTile * 2 + 16;    // f16 P row of one head (144 B)
+  static constexpr int kQSteps = kQkDim / 16;        // 36 f16 mma k-steps of Q
+};
 
 template <int MODE>
 struct Smem {
@@ -77,6 +96,7 @@ struct Smem {
 };
 static_assert(Smem<MLA_MODE_BF16>::kBytes <= 232448, "bf16 stage-1 shared memory");
 static_assert(Smem<MLA_MODE_FP8>::kBytes <= 232448, "fp8 stage-1 shared memory");
+static_assert(Smem<MLA_MODE_A16W8>::kBytes <= 232448, "a16w8 stage-1 shared memory");
 
 __device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err, 0, code); }
 
@@ -170,6 +190,22 @@ __device__ __forceinline__ void load_q(uint32_t (&qa)[Cfg<MODE>::kQSteps][4], co
       qa[s][2] = __ldg(reinterpret_cast<const uint32_t*>(q0 + k + 8));
       qa[s][3] = __ldg(reinterpret_cast<const uint32_t*>(q1 + k + 8));
     }
+  } else if constexpr (MODE == MLA_MODE_A16W8) {
+    // m16n8k16 f16 A in the permuted k order of the scores: a0 = (g, dims 4c, 4c+1),
+    // a1 = (g+8, dims 4c, 4c+1), a2 = (g, dims 4c+2, 4c+3), a3 = (g+8, dims 4c+2, 4c+3)
+    auto to_f16 = [](uint32_t bf2) -> uint32_t {
+      return ptx::pack_f16x2_sat(__uint_as_float(bf2 << 16), __uint_as_float(bf2 & 0xffff0000u));
+    };
+#pragma unroll
+    for (int s = 0; s < Cfg<MODE>::kQSteps; ++s) {
+      const int k = 16 * s + 4 * c;
+      const uint2 r0 = __ldg(reinterpret_cast<const uint2*>(q0 + k));
+      const uint2 r1 = __ldg(reinterpret_cast<const uint2*>(q1 + k));
+      qa[s][0] = to_f16(r0.x);
+      qa[s][1] = to_f16(r1.x);
+      qa[s][2] = to_f16(r0.y);
+      qa[s][3] = to_f16(r1.y);
+    }
   } else {
     // m16n8k32 e4m3 A: a0 = (g, 4c..4c+3), a1 = (g+8, 4c..), a2 = (g, 4c+16..), a3 = (g+8, 4c+16..)
     auto cast4 = [](const __nv_bfloat16* ptr) -> uint32_t {
@@ -224,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (item_has_tiles<kPaged>(w, a)) n_tiles += (w.t_end - w.t_begin + kTile - 1) / kTile;
   }
 
-  const float kv_scale = (MODE == MLA_MODE_FP8) ? __ldg(a.kv_scale) : 1.0f;
+  const float kv_scale = (MODE != MLA_MODE_BF16) ? __ldg(a.kv_scale) : 1.0f;
   const float score_log2 = a.sm_scale * kv_scale * kLog2e;  // score -> base-2 exponent
   const uint64_t policy = ptx::l2_evict_first_policy();
 
@@ -293,6 +329,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_bf16_16816(sacc, qa[2 * s2], b0, b1);
             ptx::mma_bf16_16816(sacc, qa[2 * s2 + 1], b2, b3);
           }
+        } else if constexpr (MODE == MLA_MODE_A16W8) {
+#pragma unroll
+          for (int s2 = 0; s2 < 9; ++s2) {  // 64 bytes = four 16-dim k steps per ldmatrix.x4
+            uint32_t b[4];
+            ptx::ldsm_x4(rowaddr + s2 * 64, b[0], b[1], b[2], b[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)  // b[j]: key bytes of dims 16(4 s2 + j) + 4c .. +3 of row g
+              ptx::mma_f16_16816(sacc, qa[4 * s2 + j], ptx::e4m3x2_to_f16x2(b[j] & 0xffffu),
+                                 ptx::e4m3x2_to_f16x2(b[j] >> 16));
+          }
         } else {
 #pragma unroll
           for (int s2 = 0; s2 < 9; ++s2) {  // 64 bytes = two k32 steps per ldmatrix.x4
@@ -357,6 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ps23 = __uint_as_float(u23 << 16) + __uint_as_float(u23 & 0xffff0000u);
         *reinterpret_cast<uint32_t*>(pbuf + g * C::kPStride + r0 * 2) = u01;
         *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPStride + r0 * 2) = u23;
+      } else if constexpr (MODE == MLA_MODE_A16W8) {
+        const uint32_t u01 = ptx::pack_f16x2(p0, p1), u23 = ptx::pack_f16x2(p2, p3);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&u01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&u23));
+        ps01 = f01.x + f01.y;
+        ps23 = f23.x + f23.y;
+        *reinterpret_cast<uint32_t*>(pbuf + g * C::kPStride + r0 * 2) = u01;
+        *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPStride + r0 * 2) = u23;
       } else {
         const uint32_t u01 = ptx::f32x2_to_e4m3x2(p0, p1), u23 = ptx::f32x2_to_e4m3x2(p2, p3);
         const uint32_t h01 = ptx::e4m3x2_to_f16x2(u01), h23 = ptx::e4m3x2_to_f16x2(u23);
@@ -399,28 +453,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // e4m3 V fragments of 32 rows x 32 dims: bb[h][i] holds rows 16h + 2c, +1, +8, +9 (bytes 0..3)
+        // of dim 64w + 32blk + 4g + i
+        auto v_frags = [&](int kk, int blk, uint32_t (&bb)[2][4]) {
+          const uint32_t a0 = sbase + (32 * kk + 2 * c) * C::kRowStride + 64 * warp + 32 * blk + 4 * g;
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {  // 32 rows per k step
-          uint32_t pa[4];
-          ptx::ldsm_x4(pa_addr + kk * 32, pa[0], pa[1], pa[2], pa[3]);
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t ah = a0 + 16 * h * C::kRowStride;
+            const uint32_t w0 = ptx::lds32(ah), w1 = ptx::lds32(ah + C::kRowStride);
+            const uint32_t w2 = ptx::lds32(ah + 8 * C::kRowStride), w3 = ptx::lds32(ah + 9 * C::kRowStride);
+            const uint32_t t0 = ptx::prmt(w0, w1, 0x5140), t1 = ptx::prmt(w0, w1, 0x7362);
+            const uint32_t t2 = ptx::prmt(w2, w3, 0x5140), t3 = ptx::prmt(w2, w3, 0x7362);
+            bb[h][0] = ptx::prmt(t0, t2, 0x5410);
+            bb[h][1] = ptx::prmt(t0, t2, 0x7632);
+            bb[h][2] = ptx::prmt(t1, t3, 0x5410);
+            bb[h][3] = ptx::prmt(t1, t3, 0x7632);
+          }
+        };
+        if constexpr (MODE == MLA_MODE_A16W8) {
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {  // 32 dims: n-tile i column n = dim 64w + 32blk + 4n + i
-            const uint32_t a0 = sbase + (32 * kk + 2 * c) * C::kRowStride + 64 * warp + 32 * blk + 4 * g;
-            uint32_t bb[2][4];
+          for (int kk = 0; kk < 2; ++kk) {  // 32 rows = two f16 k steps (P in row order)
+            uint32_t pa[2][4];
+            ptx::ldsm_x4(pa_addr + (2 * kk) * 32, pa[0][0], pa[0][1], pa[0][2], pa[0][3]);
+            ptx::ldsm_x4(pa_addr + (2 * kk + 1) * 32, pa[1][0], pa[1][1], pa[1][2], pa[1][3]);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // b0: mma-k 4c..4c+3 ; b1: 16 + 4c..
-              const uint32_t ah = a0 + 16 * h * C::kRowStride;
-              const uint32_t w0 = ptx::lds32(ah), w1 = ptx::lds32(ah + C::kRowStride);
-              const uint32_t w2 = ptx::lds32(ah + 8 * C::kRowStride), w3 = ptx::lds32(ah + 9 * C::kRowStride);
-              const uint32_t t0 = ptx::prmt(w0, w1, 0x5140), t1 = ptx::prmt(w0, w1, 0x7362);
-              const uint32_t t2 = ptx::prmt(w2, w3, 0x5140), t3 = ptx::prmt(w2, w3, 0x7362);
-              bb[h][0] = ptx::prmt(t0, t2, 0x5410);
-              bb[h][1] = ptx::prmt(t0, t2, 0x7632);
-              bb[h][2] = ptx::prmt(t1, t3, 0x5410);
-              bb[h][3] = ptx::prmt(t1, t3, 0x7632);
+            for (int blk = 0; blk < 2; ++blk) {  // n-tile i column n = dim 64w + 32blk + 4n + i
+              uint32_t bb[2][4];
+              v_frags(kk, blk, bb);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  ptx::mma_f16_16816(o[4 * blk + i], pa[h], ptx::e4m3x2_to_f16x2(bb[h][i] & 0xffffu),
+                                     ptx::e4m3x2_to_f16x2(bb[h][i] >> 16));
             }
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ptx::mma_e4m3_16832(o[4 * blk + i], pa, bb[0][i], bb[1][i]);
+          for (int kk = 0; kk < 2; ++kk) {  // 32 rows per k step
+            uint32_t pa[4];
+            ptx::ldsm_x4(pa_addr + kk * 32, pa[0], pa[1], pa[2], pa[3]);
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {  // 32 dims: n-tile i column n = dim 64w + 32blk + 4n + i
+              uint32_t bb[2][4];  // b0: mma-k 4c..4c+3 ; b1: 16 + 4c..
+              v_frags(kk, blk, bb);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) ptx::mma_e4m3_16832(o[4 * blk + i], pa, bb[0][i], bb[1][i]);
+            }
           }
         }
       }
@@ -555,6 +634,7 @@ int launch_stage1(int dtype_mode, const DecodeArgs& a, const DevicePlan& p, cons
   const uint8_t* z = static_cast<const uint8_t*>(zero_row);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype_mode == MLA_MODE_BF16) return launch_stage1_t<MLA_MODE_BF16>(a, p, z, s);
+  if (dtype_mode == MLA_MODE_A16W8) return launch_stage1_t<MLA_MODE_A16W8>(a, p, z, s);
   if (p.fp8_kernel == 1) return launch_stage1_t<MLA_MODE_FP8>(a, p, z, s);
   return launch_stage1_fp8_umma(a, p, stream);
 }

@@ -60,6 +60,11 @@ WORKLOADS = {
     "bf16_b128_ragged": Workload("bf16_b128_ragged", MODE_BF16, 128, (512, 8192), True, 5),
 }
 
+# Further shapes for the modes beyond the benchmark workloads: the fp8 headline shape with a bf16 query.
+EXTRA_WORKLOADS = {
+    "a16w8_b64_l8192": Workload("a16w8_b64_l8192", MODE_A16W8, 64, 8192, False, 6),
+}
+
 
 @dataclasses.dataclass
 class Inputs:
@@ -184,8 +189,12 @@ def workload_lengths(w: Workload) -> list[int]:
     return [w.kv_len] * w.batch
 
 
+def get_workload(name: str) -> Workload:
+    return WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name]
+
+
 def make_workload(name_or_w, device: str = "cpu", seed_offset: int = 0) -> Inputs:
-    w = WORKLOADS[name_or_w] if isinstance(name_or_w, str) else name_or_w
+    w = get_workload(name_or_w) if isinstance(name_or_w, str) else name_or_w
     return make_inputs(workload_lengths(w), w.mode, w.seed + seed_offset, permute=w.permute, device=device)
 
 

@@ -2,7 +2,8 @@
 element by element, on the same seeded inputs.
 
 Tolerances (max-abs error, relative L2 error of the whole output):
-bf16 2e-2 / 1e-2, fp8 6e-2 / 3e-2.
+bf16 2e-2 / 1e-2, fp8 6e-2 / 3e-2. a16w8 (bf16 Q x e4m3 KV) is held to the bf16
+bound: its products are exact (f16 x f16) and P is f16.
 """
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-TOL = {mi.MODE_BF16: (2e-2, 1e-2), mi.MODE_FP8: (6e-2, 3e-2)}
+TOL = {mi.MODE_BF16: (2e-2, 1e-2), mi.MODE_FP8: (6e-2, 3e-2), mi.MODE_A16W8: (2e-2, 1e-2)}
 
 
 @pytest.fixture(scope="module")
@@ -60,8 +61,8 @@ def oracle_out(inp: mi.Inputs, seq_ids=None):
 ODD = [1, 15, 17, 63, 64, 65, 1000, 0, 129, 2]
 
 
-MODES = [(mi.MODE_BF16, 0), (mi.MODE_FP8, 0), (mi.MODE_FP8, 1)]
-MODE_IDS = ["bf16", "fp8-tcgen05", "fp8-mma"]
+MODES = [(mi.MODE_BF16, 0), (mi.MODE_FP8, 0), (mi.MODE_FP8, 1), (mi.MODE_A16W8, 0)]
+MODE_IDS = ["bf16", "fp8-tcgen05", "fp8-mma", "a16w8"]
 
 
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
@@ -163,6 +164,8 @@ def test_host_argument_errors(mla):
     assert lib.mla_decode(*bad) == -6            # alignment
     bad = list(args); bad[7] = 1
     assert lib.mla_decode(*bad) == -1            # fp8 without kv_scale
+    bad = list(args); bad[7] = 2
+    assert lib.mla_decode(*bad) == -1            # a16w8 without kv_scale
     assert lib.mla_decode(*args) == 0
     assert plan.check_error() == 0
 
@@ -170,10 +173,12 @@ def test_host_argument_errors(mla):
 # ---------------------------------------------------------------- full-size workloads
 
 SAMPLES = {"bf16_b4_l1024": None, "fp8_b4_l8192": None, "fp8_b64_l1024": [0, 17, 38, 63],
-           "fp8_b64_l8192": [0, 21, 42, 63], "bf16_b128_ragged": [0, 31, 77, 127]}
+           "fp8_b64_l8192": [0, 21, 42, 63], "bf16_b128_ragged": [0, 31, 77, 127],
+           "a16w8_b64_l8192": [0, 25, 50, 63]}
 
 
-FULL = [(n, 0) for n in mi.WORKLOADS] + [(n, 1) for n, w in mi.WORKLOADS.items() if w.mode == mi.MODE_FP8]
+FULL = ([(n, 0) for n in mi.WORKLOADS] + [(n, 1) for n, w in mi.WORKLOADS.items() if w.mode == mi.MODE_FP8]
+        + [(n, 0) for n in mi.EXTRA_WORKLOADS])
 
 
 @pytest.mark.parametrize("name,k8", FULL, ids=[f"{n}-k{k}" for n, k in FULL])
