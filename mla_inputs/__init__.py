@@ -180,6 +180,20 @@ def make_paged_inputs(lengths, page_size: int, mode: int, seed: int, permute: bo
     return Inputs(mode, q, codes.contiguous(), scale, kv_indptr, kv_indices, SM_SCALE, ps, lp)
 
 
+def make_query_tokens(q_lens, seed: int, q_std: float = 1.0, device: str = "cpu"):
+    """Multi-token queries: q_lens[b] seeded N(0, q_std) query tokens per sequence, as a bf16
+    [sum(q_lens), 16, 576] array with row offsets qo_indptr int32 [B+1]
+    (the pages' qo_indptr = arange(B + 1) * q_seq_len, generalised to per-sequence counts)."""
+    q_lens = [int(x) for x in q_lens]
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = (torch.randn((sum(q_lens), HEADS, QK_DIM), generator=g, device=device) * q_std).to(torch.bfloat16)
+    qo = torch.zeros(len(q_lens) + 1, dtype=torch.int64)
+    if q_lens:
+        qo[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0)
+    return q, qo.to(torch.int32).to(device)
+
+
 def workload_lengths(w: Workload) -> list[int]:
     if isinstance(w.kv_len, tuple):
         g = torch.Generator()

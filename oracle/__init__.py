@@ -65,6 +65,8 @@ def _declare(lib):
     lib.oracle_decode.restype = i32
     lib.oracle_decode_paged.argtypes = [i32, P, P, i64, i32, f32, P, P, P, i32, f64, P, i32, P, P]
     lib.oracle_decode_paged.restype = i32
+    lib.oracle_decode_multi.argtypes = [i32, P, P, i64, i32, f32, P, P, P, P, i32, i32, f64, P, P]
+    lib.oracle_decode_multi.restype = i32
     lib.oracle_decode_range.argtypes = [i32, P, P, i64, i32, f32, P, P, f64, i32, i64, i64, P, P]
     lib.oracle_decode_range.restype = i32
     lib.oracle_combine.argtypes = [i32, P, P, P, P]
@@ -156,6 +158,34 @@ def decode_paged(q, kv, kv_indptr, kv_indices, kv_last_page_len, page_size: int,
                                  _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_decode_paged failed with code {rc}")
+    return out, lse
+
+
+def decode_multi(q, kv, qo_indptr, kv_indptr, kv_indices, sm_scale: float, mode: int = 0, kv_scale: float = 1.0,
+                 causal: bool = True, kv_last_page_len=None, page_size: int = 1, lib=None):
+    """Oracle multi-token decode: q [qo_indptr[B],16,576] -> (out [qo_indptr[B],16,512], lse [..,16]) float64.
+
+    Sequence b's query tokens are rows qo_indptr[b] .. qo_indptr[b+1]-1; with ``causal`` token j sees
+    the first L_b - q_b + j + 1 KV tokens. KV addressing as decode_paged (page_size 1 = rows).
+    """
+    lib = lib or load()
+    qb = _u16(q).reshape(-1)
+    kvb = _kv_bytes(kv, mode)
+    qo = _i32(qo_indptr)
+    ip = _i32(kv_indptr)
+    ix = _i32(kv_indices)
+    lp = None if kv_last_page_len is None else _i32(kv_last_page_len)
+    batch = ip.shape[0] - 1
+    n = int(qo[-1]) if batch > 0 else 0
+    out = np.zeros((n, HEADS, V_DIM), dtype=np.float64)
+    lse = np.zeros((n, HEADS), dtype=np.float64)
+    rc = lib.oracle_decode_multi(batch, _ptr(qb if qb.size else np.zeros(1, np.uint16)), _ptr(kvb), kvb.size // QK_DIM,
+                                 mode, float(kv_scale), _ptr(qo), _ptr(ip),
+                                 _ptr(ix if ix.size else np.zeros(1, np.int32)),
+                                 None if lp is None else _ptr(lp if lp.size else np.zeros(1, np.int32)),
+                                 int(page_size), int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_multi failed with code {rc}")
     return out, lse
 
 

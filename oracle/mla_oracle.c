@@ -142,19 +142,19 @@ static int64_t seq_tokens(const int32_t* kv_indptr, const int32_t* last_page_len
 }
 
 /*
- * Attention of one head of sequence b over its tokens t in [t_begin, t_end).
- * Writes out[0..511] and *lse (natural log of sum_t e^{s_t}).
+ * Attention of head h of query row q_row over the tokens t in [t_begin, t_end)
+ * of sequence b. Writes out[0..511] and *lse (natural log of sum_t e^{s_t}).
  * Returns 0, or -1 if a token's row is outside [0, num_slots).
  */
 static int attend_head(const uint16_t* q, const void* kv, int64_t num_slots, int mode, double kv_scale,
                        const int32_t* kv_indptr, const int32_t* kv_indices, int page_size, double sm_scale, int b,
-                       int h, int64_t t_begin, int64_t t_end, double* out, double* lse) {
+                       int64_t q_row, int h, int64_t t_begin, int64_t t_end, double* out, double* lse) {
   int64_t n = t_end - t_begin, t;
   int d, j;
   double m, z, *s;
   const int64_t base = (int64_t)kv_indptr[b];
   double qh[ORACLE_QK_DIM];
-  for (d = 0; d < ORACLE_QK_DIM; ++d) qh[d] = q_value(q, ((int64_t)b * ORACLE_HEADS + h) * ORACLE_QK_DIM + d, mode);
+  for (d = 0; d < ORACLE_QK_DIM; ++d) qh[d] = q_value(q, (q_row * ORACLE_HEADS + h) * ORACLE_QK_DIM + d, mode);
   for (j = 0; j < ORACLE_V_DIM; ++j) out[j] = 0.0;
   if (n <= 0) {
     *lse = -INFINITY;
@@ -217,8 +217,9 @@ int oracle_decode_paged(int batch, const uint16_t* q, const void* kv, int64_t nu
     int k = i / ORACLE_HEADS, h = i % ORACLE_HEADS;
     int b = seq_ids ? seq_ids[k] : k;
     double l;
-    int rc = attend_head(q, kv, num_rows, mode, (double)kv_scale, kv_indptr, kv_indices, page_size, sm_scale, b, h, 0,
-                         seq_tokens(kv_indptr, kv_last_page_len, page_size, b), out + (size_t)i * ORACLE_V_DIM, &l);
+    int rc = attend_head(q, kv, num_rows, mode, (double)kv_scale, kv_indptr, kv_indices, page_size, sm_scale, b, b, h,
+                         0, seq_tokens(kv_indptr, kv_last_page_len, page_size, b), out + (size_t)i * ORACLE_V_DIM,
+                         &l);
     if (rc) bad |= 1;
     if (lse) lse[i] = l;
   }
@@ -234,6 +235,62 @@ int oracle_decode(int batch, const uint16_t* q, const void* kv, int64_t num_slot
 }
 
 /*
+ * Multi-token decode (submission 690201 "V6c", _build_cache: qo_indptr =
+ * arange(B + 1) * q_seq_len, handed to the stage-1 call with max_seqlen_q).
+ * Sequence b has q_b = qo_indptr[b+1] - qo_indptr[b] query tokens, rows
+ * qo_indptr[b] .. qo_indptr[b+1] - 1 of q and out. The query tokens are the
+ * last q_b tokens of the sequence: with causal != 0, query token j sees the
+ * first max(0, L_b - q_b + j + 1) of the sequence's L_b KV tokens; otherwise
+ * every query token sees all L_b. KV addressing as oracle_decode_paged.
+ * out: [qo_indptr[B], 16, 512] float64; lse: [qo_indptr[B], 16] or NULL.
+ * Returns 0, -1 for a token row outside the buffer, -2 when out of memory,
+ * -3 for bad arguments.
+ */
+int oracle_decode_multi(int batch, const uint16_t* q, const void* kv, int64_t num_rows, int mode, float kv_scale,
+                        const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                        const int32_t* kv_last_page_len, int page_size, int causal, double sm_scale, double* out,
+                        double* lse) {
+  int b, bad = 0;
+  int64_t i, n_rows, *row_seq, *row_len;
+  if (batch < 0 || mode < 0 || mode > 2 || page_size < 1 || !out || !qo_indptr) return -3;
+  if (batch > 0 && qo_indptr[0] != 0) return -3;
+  for (b = 0; b < batch; ++b)
+    if (qo_indptr[b + 1] < qo_indptr[b] || seq_tokens(kv_indptr, kv_last_page_len, page_size, b) < 0) return -3;
+  n_rows = batch > 0 ? qo_indptr[batch] : 0;
+  row_seq = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_rows + 1));
+  row_len = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_rows + 1));
+  if (!row_seq || !row_len) {
+    free(row_seq);
+    free(row_len);
+    return -2;
+  }
+  /* sequence and number of visible KV tokens of every query row */
+  for (b = 0; b < batch; ++b) {
+    const int64_t L = seq_tokens(kv_indptr, kv_last_page_len, page_size, b);
+    const int64_t qb = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+    int64_t j;
+    for (j = 0; j < qb; ++j) {
+      int64_t n = causal ? L - qb + j + 1 : L;
+      row_seq[qo_indptr[b] + j] = b;
+      row_len[qo_indptr[b] + j] = n < 0 ? 0 : (n > L ? L : n);
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (i = 0; i < n_rows * ORACLE_HEADS; ++i) {
+    const int64_t r = i / ORACLE_HEADS;
+    const int h = (int)(i % ORACLE_HEADS);
+    double l;
+    int rc = attend_head(q, kv, num_rows, mode, (double)kv_scale, kv_indptr, kv_indices, page_size, sm_scale,
+                         (int)row_seq[r], r, h, 0, row_len[r], out + (size_t)i * ORACLE_V_DIM, &l);
+    if (rc) bad |= 1;
+    if (lse) lse[i] = l;
+  }
+  free(row_seq);
+  free(row_len);
+  return bad ? -1 : 0;
+}
+
+/*
  * Attention of sequence b over its rows [t_begin, t_end) only: the partial
  * result one split of a split-KV decode must produce. out [16,512], lse [16].
  */
@@ -246,7 +303,8 @@ int oracle_decode_range(int batch, const uint16_t* q, const void* kv, int64_t nu
   len = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
   if (t_begin < 0 || t_end > len || t_begin > t_end) return -3;
   for (h = 0; h < ORACLE_HEADS; ++h)
-    if (attend_head(q, kv, num_slots, mode, (double)kv_scale, kv_indptr, kv_indices, 1, sm_scale, b, h, t_begin, t_end,
+    if (attend_head(q, kv, num_slots, mode, (double)kv_scale, kv_indptr, kv_indices, 1, sm_scale, b, b, h, t_begin,
+                    t_end,
                     out + (size_t)h * ORACLE_V_DIM, lse + h))
       bad = 1;
   return bad ? -1 : 0;

@@ -8,6 +8,7 @@ library handle so the planted-mistake test can run them on mutated copies.
 from __future__ import annotations
 
 import math
+import warnings
 
 import numpy as np
 import torch
@@ -352,10 +353,107 @@ def pin_paged_errors(lib):
     raise AssertionError("page id past the buffer was not reported")
 
 
+# ---------------------------------------------------------------- multi-token decode
+
+def _gather_kv(inp: mi.Inputs, b: int, L: int) -> torch.Tensor:
+    """Sequence b's first L KV tokens as float64 [L, 576]: row indices, or the page view."""
+    kvv = _torch_kv_values(inp)
+    ip = inp.kv_indptr.tolist()
+    if inp.page_size == 1:
+        return kvv[inp.kv_indices[ip[b]:ip[b + 1]].long()][:L]
+    return kvv.view(-1, inp.page_size, D)[inp.kv_indices[ip[b]:ip[b + 1]].long()].reshape(-1, D)[:L]
+
+
+def sdpa_reference_multi(inp: mi.Inputs, q, qo, lengths, causal: bool):
+    """torch float64 SDPA per sequence: its query rows against its KV tokens, masked with torch's
+    lower-right causal bias when ``causal`` (the query tokens are the sequence's last ones)."""
+    from torch.nn.attention.bias import causal_lower_right
+    if inp.mode == mi.MODE_FP8:
+        qv = q.to(torch.float8_e4m3fn).to(torch.float64)
+    else:
+        qv = q.to(torch.float64)
+    qo = qo.tolist()
+    outs, lses = [], []
+    for b, L in enumerate(lengths):
+        qb = qv[qo[b]:qo[b + 1]]                      # [n, 576]
+        n = qb.shape[0]
+        if n == 0:
+            continue
+        k = _gather_kv(inp, b, L)
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            mask = (causal_lower_right(n, L)._materialize(torch.device("cpu")) if causal
+                    else torch.ones(n, L, dtype=torch.bool))
+        for h in range(H):
+            sh = torch.einsum("nd,td->nt", qb[:, h], k) * inp.sm_scale
+            sh = sh.masked_fill(~mask, -math.inf)
+            lse = torch.logsumexp(sh, dim=1)
+            with warnings.catch_warnings():  # rows with no visible key give NaN there; zeroed below
+                warnings.simplefilter("ignore")
+                o = torch.nn.functional.scaled_dot_product_attention(
+                    qb[None, None, :, h], k[None, None], k[None, None, :, :DV], attn_mask=mask[None, None],
+                    scale=inp.sm_scale)[0, 0]
+            o = torch.where(torch.isinf(lse)[:, None], torch.zeros_like(o), o)
+            outs.append((qo[b], h, o))
+            lses.append((qo[b], h, lse))
+    total = qo[-1]
+    out = torch.zeros(total, H, DV, dtype=torch.float64)
+    lse_all = torch.zeros(total, H, dtype=torch.float64)
+    for r0, h, o in outs:
+        out[r0:r0 + o.shape[0], h] = o
+    for r0, h, l in lses:
+        lse_all[r0:r0 + l.shape[0], h] = l
+    return out.numpy(), lse_all.numpy()
+
+
+def _dec_multi(inp, q, qo, causal, lib):
+    return oracle.decode_multi(q, inp.kv, qo, inp.kv_indptr, inp.kv_indices, inp.sm_scale, inp.mode, inp.kv_scale,
+                               causal=causal, kv_last_page_len=inp.kv_last_page_len, page_size=inp.page_size, lib=lib)
+
+
+def pin_multi_single_token(lib):
+    """One query token per sequence, causal or not, is the single-token decode."""
+    inp = _inputs([1, 9, 40], 1, seed=14, permute=True, extra_slots=3)
+    out, lse = _dec(inp, lib)
+    qo = torch.arange(inp.batch + 1, dtype=torch.int32)
+    for causal in (False, True):
+        out2, lse2 = _dec_multi(inp, inp.q, qo, causal, lib)
+        assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def pin_multi_library_sdpa(lib):
+    """Several query tokens per sequence against torch float64 SDPA with and without the lower-right
+    causal mask: row addressing and paged, all modes."""
+    lengths, q_lens = [5, 40, 17, 64, 3], [1, 3, 4, 2, 3]
+    for mode in (0, 1, 2):
+        for paged in (False, True):
+            inp = (_paged(lengths, 8, mode, seed=60 + mode, permute=True, extra_pages=2) if paged
+                   else _inputs(lengths, mode, seed=60 + mode, permute=True, extra_slots=7))
+            q, qo = mi.make_query_tokens(q_lens, seed=70 + mode, q_std=2.0)
+            for causal in (False, True):
+                out, lse = _dec_multi(inp, q, qo, causal, lib)
+                ref, ref_lse = sdpa_reference_multi(inp, q, qo, lengths, causal)
+                np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+                np.testing.assert_allclose(lse, ref_lse, rtol=1e-11, atol=1e-12)
+
+
+def pin_multi_more_queries_than_tokens(lib):
+    """Causal, with more query tokens than KV tokens: the first q_b - L_b query tokens see nothing
+    (zeros, LSE -inf); the others see their prefix."""
+    lengths, q_lens = [2, 6], [5, 6]
+    inp = _inputs(lengths, 0, seed=17)
+    q, qo = mi.make_query_tokens(q_lens, seed=18)
+    out, lse = _dec_multi(inp, q, qo, True, lib)
+    assert np.all(out[:3] == 0) and np.all(np.isneginf(lse[:3]))
+    ref, ref_lse = sdpa_reference_multi(inp, q, qo, lengths, True)
+    np.testing.assert_allclose(out[3:], ref[3:], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse[3:], ref_lse[3:], rtol=1e-11, atol=1e-12)
+
+
 ALL_PINS = [
     pin_bf16_decode, pin_e4m3_decode_table, pin_e4m3_encode_vs_torch, pin_e4m3_encode_saturates,
     pin_single_row, pin_identical_rows, pin_uniform_scores, pin_two_rows, pin_convex_hull,
     pin_permutation, pin_library_sdpa, pin_split_combine, pin_empty_and_errors,
     pin_paged_library_sdpa, pin_paged_unit_pages, pin_paged_permutation, pin_paged_unused_rows_ignored,
-    pin_paged_errors,
+    pin_paged_errors, pin_multi_single_token, pin_multi_library_sdpa, pin_multi_more_queries_than_tokens,
 ]

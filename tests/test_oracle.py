@@ -31,7 +31,9 @@ MUTANTS = {
     "q_cast_skipped": ("if (mode == 1) v = oracle_e4m3_decode(oracle_e4m3_encode(v));", ""),
     "missing_normalisation": ("double w = s[t] / z;", "double w = s[t];"),
     "missing_sm_scale": ("s[t] = sm_scale * acc;", "s[t] = acc;"),
-    "wrong_head": ("((int64_t)b * ORACLE_HEADS + h) * ORACLE_QK_DIM", "((int64_t)b * ORACLE_HEADS + 0) * ORACLE_QK_DIM"),
+    "wrong_head": ("(q_row * ORACLE_HEADS + h) * ORACLE_QK_DIM", "(q_row * ORACLE_HEADS + 0) * ORACLE_QK_DIM"),
+    "causal_off_by_one": ("int64_t n = causal ? L - qb + j + 1 : L;", "int64_t n = causal ? L - qb + j : L;"),
+    "query_row_of_sequence": ("(int)row_seq[r], r, h, 0, row_len[r]", "(int)row_seq[r], row_seq[r], h, 0, row_len[r]"),
     "indices_ignored": ("return (int64_t)kv_indices[page_base + t / page_size] * page_size + t % page_size;",
                         "return page_base * page_size + t;"),
     "page_offset_dropped": ("* page_size + t % page_size;", "* page_size;"),
