@@ -298,6 +298,49 @@ int mla_plan_compute_host_paged(int batch, const int32_t* kv_indptr_host, const 
                                 int page_size, int num_sms, const mla_plan_options* options, int32_t* counts,
                                 int32_t* items, int items_cap, int32_t* work_indptr, int indptr_cap,
                                 int32_t* reduce, int reduce_cap);
+/*
+ * Several query tokens per sequence (the pages' qo_indptr / max_seqlen_q:
+ * submission 690201 "V6c", _build_cache builds qo_indptr = arange(B+1) *
+ * q_seq_len for the stage-1 call; is_causal is set in 689529 "V3",
+ * _get_or_build_cache). Sequence b has q_b = qo_indptr[b+1] - qo_indptr[b]
+ * query tokens, rows qo_indptr[b] .. qo_indptr[b+1]-1 of q [qo_indptr[B],16,576]
+ * and out [qo_indptr[B],16,512]. They are the sequence's last q_b tokens: with
+ * causal != 0, query token j attends to the first max(0, L_b - q_b + j + 1) of
+ * the sequence's L_b KV tokens (the lower-right-aligned causal mask), else to
+ * all of them. A query token that sees no KV token gets zeros. KV addressing is
+ * the paged layout above; page_size 1 with kv_last_page_len NULL is plain row
+ * addressing.
+ *
+ * The work is planned per sequence: one CTA processes every query token of a
+ * sequence on the same KV rows back to back, so a row is read from HBM once
+ * and from L2 for the other tokens.
+ *
+ * mla_decode_plan_multi — the planner for that layout (host arrays as for
+ *   mla_decode_plan_paged, plus qo_indptr_host [B+1], 0 first, non-decreasing).
+ *   A multi-token plan serves only mla_decode_multi with the same page_size.
+ *   Errors as mla_decode_plan_paged, MLA_ERR_INDPTR also for a bad qo_indptr.
+ */
+int mla_decode_plan_multi(int batch, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                          const int32_t* kv_last_page_len_host, int page_size, int causal, int num_sms,
+                          const mla_plan_options* options, mla_plan** plan_out);
+/*
+ * mla_decode_multi — decode of every query token.
+ *   q          device bf16 [qo_indptr[B], 16, 576]; out device bf16 [qo_indptr[B], 16, 512].
+ *   qo_indptr  device int32 [B+1], equal to the plan's (the kernel checks each
+ *              item's query row against it and records MLA_ERR_PLAN_MISMATCH,
+ *              skipping that work, if not).
+ *   Other arguments, ownership, ordering and errors as mla_decode_paged.
+ */
+int mla_decode_multi(const void* q, const void* kv, const float* kv_scale, const int32_t* qo_indptr,
+                     const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                     int page_size, void* out, float sm_scale, int dtype_mode, mla_plan* workspace, void* stream);
+/* mla_plan_compute_host for multi-token plans: items as int32 [items_cap][7] =
+   (sequence, first token, end token, partial slot or -1, sequence length,
+   query row, query token within the sequence). */
+int mla_plan_compute_host_multi(int batch, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                                const int32_t* kv_last_page_len_host, int page_size, int causal, int num_sms,
+                                const mla_plan_options* options, int32_t* counts, int32_t* items, int items_cap,
+                                int32_t* work_indptr, int indptr_cap, int32_t* reduce, int reduce_cap);
 /* Human-readable name of a status code (static string). */
 const char* mla_strerror(int status);
 

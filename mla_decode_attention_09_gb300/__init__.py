@@ -42,7 +42,7 @@ EXPORTS = (
     "mla_decode_plan", "mla_decode_plan_ex", "mla_plan_release", "mla_plan_get_info", "mla_decode",
     "mla_decode_stage1", "mla_decode_reduce", "mla_plan_check_error", "mla_strerror", "mla_version",
     "mla_plan_compute_host", "mla_decode_noalloc", "mla_decode_plan_paged", "mla_decode_paged",
-    "mla_plan_compute_host_paged",
+    "mla_plan_compute_host_paged", "mla_decode_plan_multi", "mla_decode_multi", "mla_plan_compute_host_multi",
 )
 
 
@@ -100,6 +100,10 @@ def load_library(path: str | None = None):
         lib.mla_decode_paged.argtypes = [V, V, V, V, V, V, I, V, F, I, V, V]
         lib.mla_plan_compute_host_paged.argtypes = [I, V, V, I, I, ctypes.POINTER(PlanOptions), V, V, I, V, I, V,
                                                     I]
+        lib.mla_decode_plan_multi.argtypes = [I, V, V, V, I, I, I, ctypes.POINTER(PlanOptions), ctypes.POINTER(V)]
+        lib.mla_decode_multi.argtypes = [V, V, V, V, V, V, V, I, V, F, I, V, V]
+        lib.mla_plan_compute_host_multi.argtypes = [I, V, V, V, I, I, I, ctypes.POINTER(PlanOptions), V, V, I, V, I,
+                                                    V, I]
         for name in EXPORTS:
             if name not in ("mla_strerror",):
                 getattr(lib, name).restype = I
@@ -139,16 +143,27 @@ class Plan:
     """
 
     def __init__(self, kv_indptr_host, num_sms: int = 0, *, page_size: int | None = None,
-                 kv_last_page_len_host=None, **options):
+                 kv_last_page_len_host=None, qo_indptr_host=None, causal: bool = True, **options):
         lib = load_library()
         ip = _host_indptr(kv_indptr_host)
         self.batch = ip.numel() - 1
         self._lib = lib
         self._handle = ctypes.c_void_p()
         o = _opts(**options)
-        self.paged = page_size is not None
-        self.page_size = int(page_size) if self.paged else 1
-        if self.paged:
+        self.multi = qo_indptr_host is not None
+        self.paged = page_size is not None and not self.multi
+        self.page_size = int(page_size) if page_size is not None else 1
+        self.causal = bool(causal)
+        if self.multi:
+            qo = _host_indptr(qo_indptr_host)
+            lp = None if kv_last_page_len_host is None else _host_indptr(kv_last_page_len_host)
+            _check(lib.mla_decode_plan_multi(self.batch, qo.data_ptr(), ip.data_ptr(),
+                                             None if lp is None else lp.data_ptr(), self.page_size,
+                                             int(self.causal), int(num_sms), ctypes.byref(o),
+                                             ctypes.byref(self._handle)), "mla_decode_plan_multi")
+            self.qo_indptr_host = qo
+            self.num_q_rows = int(qo[-1]) if self.batch > 0 else 0
+        elif self.paged:
             lp = None if kv_last_page_len_host is None else _host_indptr(kv_last_page_len_host)
             _check(lib.mla_decode_plan_paged(self.batch, ip.data_ptr(), None if lp is None else lp.data_ptr(),
                                              self.page_size, int(num_sms), ctypes.byref(o),
@@ -194,6 +209,13 @@ def plan_paged(kv_indptr_host, kv_last_page_len_host, page_size: int, num_sms: i
     ``kv_last_page_len_host`` [B] the tokens used in each sequence's last page."""
     return Plan(kv_indptr_host, num_sms, page_size=page_size, kv_last_page_len_host=kv_last_page_len_host,
                 **options)
+
+
+def plan_multi(qo_indptr_host, kv_indptr_host, num_sms: int = 0, *, causal: bool = True, page_size: int = 1,
+               kv_last_page_len_host=None, **options) -> Plan:
+    """Plan for several query tokens per sequence (rows qo_indptr[b] .. of q and out)."""
+    return Plan(kv_indptr_host, num_sms, page_size=page_size, kv_last_page_len_host=kv_last_page_len_host,
+                qo_indptr_host=qo_indptr_host, causal=causal, **options)
 
 
 def _stream_ptr(stream) -> int | None:
@@ -278,6 +300,38 @@ def decode_paged(q, kv, kv_scale, kv_indptr, kv_indices, kv_last_page_len, page_
     return out
 
 
+def decode_multi(q, kv, kv_scale, qo_indptr, kv_indptr, kv_indices, out=None, *, plan: Plan,
+                 kv_last_page_len=None, sm_scale: float = SM_SCALE, dtype_mode=None, stream=None,
+                 validate: bool = True) -> torch.Tensor:
+    """Decode of several query tokens per sequence: q bf16 [qo_indptr[B],16,576] -> out bf16
+    [qo_indptr[B],16,512], with a plan from plan_multi (its page size and causal flag apply)."""
+    mode = _mode_of(kv) if dtype_mode is None else int(dtype_mode)
+    if out is None:
+        out = torch.empty((plan.num_q_rows, HEADS, V_DIM), dtype=torch.bfloat16, device=q.device)
+    if validate:
+        if not plan.multi:
+            raise ValueError("decode_multi needs a plan from plan_multi")
+        if q.dtype != torch.bfloat16 or tuple(q.shape) != (plan.num_q_rows, HEADS, QK_DIM):
+            raise ValueError(f"q must be bf16 [{plan.num_q_rows},{HEADS},{QK_DIM}]")
+        if out.dtype != torch.bfloat16 or tuple(out.shape) != (plan.num_q_rows, HEADS, V_DIM):
+            raise ValueError(f"out must be bf16 [{plan.num_q_rows},{HEADS},{V_DIM}]")
+        for name, t in (("q", q), ("kv", kv), ("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr),
+                        ("kv_indices", kv_indices), ("out", out)):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if qo_indptr.dtype != torch.int32 or qo_indptr.numel() != plan.batch + 1:
+            raise ValueError("qo_indptr must be int32 [B+1]")
+        if mode != MODE_BF16 and (kv_scale is None or kv_scale.dtype != torch.float32 or not kv_scale.is_cuda):
+            raise ValueError("fp8 KV needs kv_scale as a float32 CUDA tensor of one element")
+    ks = kv_scale.data_ptr() if kv_scale is not None else None
+    lp = kv_last_page_len.data_ptr() if kv_last_page_len is not None else None
+    _check(load_library().mla_decode_multi(q.data_ptr(), kv.data_ptr(), ks, qo_indptr.data_ptr(), kv_indptr.data_ptr(),
+                                           kv_indices.data_ptr(), lp, int(plan.page_size), out.data_ptr(),
+                                           float(sm_scale), int(mode), plan.handle, _stream_ptr(stream)),
+           "mla_decode_multi")
+    return out
+
+
 def decode_stage1(q, kv, kv_scale, kv_indptr, kv_indices, out, *, plan: Plan, sm_scale: float = SM_SCALE,
                   dtype_mode=None, stream=None) -> torch.Tensor:
     """Only the persistent stage-1 kernel (final rows of unsplit sequences + partials)."""
@@ -339,6 +393,33 @@ def plan_compute_host_paged(kv_indptr_host, kv_last_page_len_host, page_size: in
                                            counts.ctypes.data, items.ctypes.data, items.shape[0], wip.ctypes.data,
                                            wip.shape[0], red.ctypes.data, red.shape[0]),
            "mla_plan_compute_host_paged")
+    return {"items": items[:n_items], "work_indptr": wip, "reduce": red[:n_reduce], "num_ctas": n_ctas,
+            "num_slots": n_slots}
+
+
+def plan_compute_host_multi(qo_indptr_host, kv_indptr_host, num_sms: int, *, causal: bool = True,
+                            page_size: int = 1, kv_last_page_len_host=None, **options) -> dict:
+    """plan_compute_host for multi-token plans; items have 7 fields (..., query row, query token)."""
+    import numpy as np
+
+    lib = load_library()
+    qo = _host_indptr(qo_indptr_host)
+    ip = _host_indptr(kv_indptr_host)
+    lp = None if kv_last_page_len_host is None else _host_indptr(kv_last_page_len_host)
+    lpp = None if lp is None else lp.data_ptr()
+    batch = ip.numel() - 1
+    o = _opts(**options)
+    counts = np.zeros(4, dtype=np.int32)
+    args = (batch, qo.data_ptr(), ip.data_ptr(), lpp, int(page_size), int(bool(causal)), int(num_sms), ctypes.byref(o))
+    _check(lib.mla_plan_compute_host_multi(*args, counts.ctypes.data, None, 0, None, 0, None, 0),
+           "mla_plan_compute_host_multi")
+    n_items, n_ctas, n_slots, n_reduce = (int(x) for x in counts)
+    items = np.zeros((max(n_items, 1), 7), dtype=np.int32)
+    wip = np.zeros(n_ctas + 1, dtype=np.int32)
+    red = np.zeros((max(n_reduce, 1), 3), dtype=np.int32)
+    _check(lib.mla_plan_compute_host_multi(*args, counts.ctypes.data, items.ctypes.data, items.shape[0],
+                                           wip.ctypes.data, wip.shape[0], red.ctypes.data, red.shape[0]),
+           "mla_plan_compute_host_multi")
     return {"items": items[:n_items], "work_indptr": wip, "reduce": red[:n_reduce], "num_ctas": n_ctas,
             "num_slots": n_slots}
 

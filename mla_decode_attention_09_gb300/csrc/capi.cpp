@@ -17,10 +17,12 @@ struct mla_plan {
   int batch = 0;
   int num_sms = 0;
   mla::PlanOptions opt;
-  bool paged = false;            // built by mla_decode_plan_paged: serves mla_decode_paged only
+  int kind = 0;                  // Layout kind the plan was built for; serves only that decode call
   int page_size = 1;
+  bool causal = false;
   std::vector<int32_t> indptr;   // cache key contents
   std::vector<int32_t> last_page_len;
+  std::vector<int32_t> qo_indptr;
   mla::HostPlan host;
   mla::DevicePlan dev{};
   void* block = nullptr;         // single device allocation backing every buffer
@@ -35,25 +37,34 @@ std::vector<mla_plan*> g_cache;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Layout a plan is built for: row addressing, or pages of page_size tokens
-// with the last page lengths `last` (NULL when page_size is 1).
+// Layout a plan is built for, and that a decode call passes: row addressing
+// (kRowsKind), pages of page_size tokens with last page lengths `last` (NULL
+// when page_size is 1), or several query tokens per sequence (rows qo[b] ..
+// qo[b+1]-1, causal or not) over either KV addressing. For plans the arrays
+// are host copies; for decode calls, the device arrays.
+enum { kRowsKind = 0, kPagedKind = 1, kMultiKind = 2 };
 struct Layout {
-  bool paged;
+  int kind;
   int page_size;
   const int32_t* last;
+  const int32_t* qo;
+  bool causal;
 };
+
+bool same_array(const std::vector<int32_t>& v, const int32_t* a, size_t n) {
+  if (a == nullptr || n == 0) return v.empty();
+  return v.size() == n && std::memcmp(v.data(), a, sizeof(int32_t) * n) == 0;
+}
 
 bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, const Layout& l, int num_sms,
               const mla::PlanOptions& o) {
-  if (!(p->device == device && p->batch == batch && p->num_sms == num_sms && p->paged == l.paged &&
-        p->page_size == l.page_size && p->opt.num_kv_slots == o.num_kv_slots &&
-        p->opt.min_rows_per_split == o.min_rows_per_split && p->opt.granularity == o.granularity &&
-        p->opt.ctas_per_sm == o.ctas_per_sm && p->opt.fp8_kernel == o.fp8_kernel &&
-        std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0))
-    return false;
-  if (p->last_page_len.empty() != (l.last == nullptr || batch == 0)) return false;
-  return l.last == nullptr || batch == 0 ||
-         std::memcmp(p->last_page_len.data(), l.last, sizeof(int32_t) * (size_t)batch) == 0;
+  return p->device == device && p->batch == batch && p->num_sms == num_sms && p->kind == l.kind &&
+         p->page_size == l.page_size && p->causal == l.causal && p->opt.num_kv_slots == o.num_kv_slots &&
+         p->opt.min_rows_per_split == o.min_rows_per_split && p->opt.granularity == o.granularity &&
+         p->opt.ctas_per_sm == o.ctas_per_sm && p->opt.fp8_kernel == o.fp8_kernel &&
+         std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0 &&
+         same_array(p->last_page_len, l.last, (size_t)batch) &&
+         same_array(p->qo_indptr, l.qo, batch > 0 ? (size_t)batch + 1 : 0);
 }
 
 void destroy_plan(mla_plan* p) {
@@ -88,12 +99,18 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   p->batch = batch;
   p->num_sms = num_sms;
   p->opt = opt;
-  p->paged = l.paged;
+  p->kind = l.kind;
   p->page_size = l.page_size;
+  p->causal = l.causal;
   p->indptr.assign(kv_indptr_host, kv_indptr_host + batch + 1);
   if (l.last && batch > 0) p->last_page_len.assign(l.last, l.last + batch);
-  int rc = l.paged ? mla::build_host_plan_paged(batch, kv_indptr_host, l.last, l.page_size, num_sms, opt, &p->host)
-                   : mla::build_host_plan(batch, kv_indptr_host, num_sms, opt, &p->host);
+  if (l.qo && batch > 0) p->qo_indptr.assign(l.qo, l.qo + batch + 1);
+  int rc = l.kind == kMultiKind
+               ? mla::build_host_plan_multi(batch, l.qo, kv_indptr_host, l.last, l.page_size, l.causal, num_sms, opt,
+                                            &p->host)
+           : l.kind == kPagedKind ? mla::build_host_plan_paged(batch, kv_indptr_host, l.last, l.page_size, num_sms, opt,
+                                                               &p->host)
+                                  : mla::build_host_plan(batch, kv_indptr_host, num_sms, opt, &p->host);
   if (rc != MLA_OK) {
     delete p;
     return rc;
@@ -153,8 +170,9 @@ int validate_decode(const void* q, const void* kv, const float* kv_scale, const 
                     const int32_t* kv_indices, const void* out, int dtype_mode, const mla_plan* plan,
                     const Layout& l) {
   if (!plan || plan->refcount <= 0) return MLA_ERR_ARG;
-  if (plan->paged != l.paged || plan->page_size != l.page_size) return MLA_ERR_ARG;
-  if (l.paged && l.page_size > 1 && plan->batch > 0 && !l.last) return MLA_ERR_ARG;
+  if (plan->kind != l.kind || plan->page_size != l.page_size) return MLA_ERR_ARG;
+  if (l.page_size > 1 && plan->batch > 0 && !l.last) return MLA_ERR_ARG;
+  if (l.kind == kMultiKind && plan->batch > 0 && !l.qo) return MLA_ERR_ARG;
   if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8 && dtype_mode != MLA_MODE_A16W8)
     return MLA_ERR_DTYPE;
   if (plan->batch > 0) {
@@ -174,6 +192,7 @@ int plan_common(int batch, const int32_t* kv_indptr_host, const Layout& layout, 
   try {
     if (!plan_out || batch < 0 || (!kv_indptr_host && batch > 0)) return MLA_ERR_ARG;
     if (layout.page_size < 1 || (layout.page_size > 1 && batch > 0 && !layout.last)) return MLA_ERR_ARG;
+    if (layout.kind == kMultiKind && batch > 0 && !layout.qo) return MLA_ERR_ARG;
     *plan_out = nullptr;
     int device = -1;
     int rc = check_device(&device);
@@ -213,7 +232,7 @@ int decode_common(const mla::DecodeArgs& a, int dtype_mode, mla_plan* workspace,
   return MLA_OK;
 }
 
-constexpr Layout kRows{false, 1, nullptr};
+constexpr Layout kRows{kRowsKind, 1, nullptr, nullptr, false};
 
 }  // namespace
 
@@ -226,7 +245,15 @@ int mla_decode_plan_ex(int batch, const int32_t* kv_indptr_host, int num_sms, co
 
 int mla_decode_plan_paged(int batch, const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
                           int page_size, int num_sms, const mla_plan_options* options, mla_plan** plan_out) {
-  const Layout l{true, page_size, page_size > 1 ? kv_last_page_len_host : nullptr};
+  const Layout l{kPagedKind, page_size, page_size > 1 ? kv_last_page_len_host : nullptr, nullptr, false};
+  return plan_common(batch, kv_indptr_host, l, num_sms, options, plan_out);
+}
+
+int mla_decode_plan_multi(int batch, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                          const int32_t* kv_last_page_len_host, int page_size, int causal, int num_sms,
+                          const mla_plan_options* options, mla_plan** plan_out) {
+  const Layout l{kMultiKind, page_size, page_size > 1 ? kv_last_page_len_host : nullptr, qo_indptr_host,
+                 causal != 0};
   return plan_common(batch, kv_indptr_host, l, num_sms, options, plan_out);
 }
 
@@ -293,12 +320,26 @@ int mla_decode_paged(const void* q, const void* kv, const float* kv_scale, const
                      const int32_t* kv_indices, const int32_t* kv_last_page_len, int page_size, void* out,
                      float sm_scale, int dtype_mode, mla_plan* workspace, void* stream) {
   if (page_size < 1) return MLA_ERR_ARG;
-  const Layout l{true, page_size, page_size > 1 ? kv_last_page_len : nullptr};
+  const Layout l{kPagedKind, page_size, page_size > 1 ? kv_last_page_len : nullptr, nullptr, false};
   int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace, l);
   if (rc != MLA_OK) return rc;
   mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
   a.kv_last_page_len = l.last;
   a.page_size = page_size;
+  return decode_common(a, dtype_mode, workspace, stream, true);
+}
+
+int mla_decode_multi(const void* q, const void* kv, const float* kv_scale, const int32_t* qo_indptr,
+                     const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                     int page_size, void* out, float sm_scale, int dtype_mode, mla_plan* workspace, void* stream) {
+  if (page_size < 1 || !workspace) return MLA_ERR_ARG;
+  const Layout l{kMultiKind, page_size, page_size > 1 ? kv_last_page_len : nullptr, qo_indptr, workspace->causal};
+  int rc = validate_decode(q, kv, kv_scale, kv_indptr, kv_indices, out, dtype_mode, workspace, l);
+  if (rc != MLA_OK) return rc;
+  mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
+  a.kv_last_page_len = l.last;
+  a.page_size = page_size;
+  a.qo_indptr = qo_indptr;
   return decode_common(a, dtype_mode, workspace, stream, true);
 }
 
@@ -372,6 +413,36 @@ int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms,
     const int rc = mla::build_host_plan(batch, batch > 0 ? kv_indptr_host : &kZero, num_sms,
                                         mla::resolve_options(options), &h);
     return export_host_plan(rc, h, counts4, items5, items_cap, work_indptr, indptr_cap, reduce3, reduce_cap);
+  } catch (...) {
+    return MLA_ERR_NOMEM;
+  }
+}
+
+int mla_plan_compute_host_multi(int batch, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                                const int32_t* kv_last_page_len_host, int page_size, int causal, int num_sms,
+                                const mla_plan_options* options, int32_t* counts4, int32_t* items7, int items_cap,
+                                int32_t* work_indptr, int indptr_cap, int32_t* reduce3, int reduce_cap) {
+  try {
+    if (!counts4) return MLA_ERR_ARG;
+    mla::HostPlan h;
+    static const int32_t kZero = 0;
+    const int rc = mla::build_host_plan_multi(batch, batch > 0 ? qo_indptr_host : &kZero,
+                                              batch > 0 ? kv_indptr_host : &kZero, kv_last_page_len_host, page_size,
+                                              causal != 0, num_sms, mla::resolve_options(options), &h);
+    if (rc == MLA_OK && items7 && items_cap >= h.n_items)
+      for (int i = 0; i < h.n_items; ++i) {
+        items7[7 * i + 5] = h.items[i].q_row;
+        items7[7 * i + 6] = h.items[i].q_tok;
+      }
+    // the first five fields of every item, at a stride of seven
+    std::vector<int32_t> five(items7 && rc == MLA_OK && items_cap >= h.n_items ? (size_t)h.n_items * 5 : 0);
+    const int n_items = rc == MLA_OK ? h.n_items : 0;
+    const int rc2 = export_host_plan(rc, h, counts4, five.empty() ? nullptr : five.data(), items_cap, work_indptr,
+                                     indptr_cap, reduce3, reduce_cap);
+    if (rc2 == MLA_OK && !five.empty())
+      for (int i = 0; i < n_items; ++i)
+        for (int f = 0; f < 5; ++f) items7[7 * i + f] = five[(size_t)i * 5 + f];
+    return rc2;
   } catch (...) {
     return MLA_ERR_NOMEM;
   }

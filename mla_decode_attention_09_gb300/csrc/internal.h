@@ -12,22 +12,28 @@ constexpr int kHeads = MLA_NUM_HEADS;     // 16 query heads share one KV head
 constexpr int kQkDim = MLA_QK_HEAD_DIM;   // 576 = 512 latent + 64 rope
 constexpr int kVDim = MLA_V_HEAD_DIM;     // 512: value = first 512 entries of the KV row
 
-// One unit of stage-1 work: tokens [t_begin, t_end) of sequence b (offsets
-// relative to the sequence start). slot >= 0: write normalised fp32 partial O
-// and LSE to workspace slot `slot`; slot < 0: the item covers the whole
-// sequence and writes final bf16 output. seq_len is the token count the plan
-// saw, checked against the device kv_indptr (and last page lengths).
+// One unit of stage-1 work: query row q_row attends to KV tokens
+// [t_begin, t_end) of sequence b (offsets relative to the sequence start).
+// slot >= 0: write normalised fp32 partial O and LSE to workspace slot
+// `slot`; slot < 0: the item covers every token the query row sees and writes
+// its final bf16 output. seq_len is the token count the plan saw, checked
+// against the device kv_indptr (and last page lengths); q_tok is the query
+// token's index within its sequence, checked against the device qo_indptr.
+// Single-token plans have q_row = b and q_tok = 0.
 struct WorkItem {
   int32_t b;
   int32_t t_begin;
   int32_t t_end;
   int32_t slot;
   int32_t seq_len;
-  int32_t pad[3];
+  int32_t q_row;
+  int32_t q_tok;
+  int32_t pad;
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
-// One split sequence for the reduce: slots [slot_begin, slot_begin + n_slots).
+// One split query row for the reduce: slots [slot_begin, slot_begin + n_slots),
+// merged into output row b.
 struct ReduceEntry {
   int32_t b;
   int32_t slot_begin;
@@ -69,6 +75,14 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
 // last_page_len[b] (1..page_size) gives the tokens used in b's last page.
 int build_host_plan_paged(int batch, const int32_t* kv_indptr, const int32_t* last_page_len, int page_size,
                           int num_sms, const PlanOptions& opt, HostPlan* out);
+// Several query tokens per sequence: rows qo_indptr[b] .. qo_indptr[b+1]-1 of
+// q and out. With causal, query token j of a sequence with q_b query tokens
+// and L_b KV tokens sees its first max(0, L_b - q_b + j + 1) tokens; else all.
+// KV addressing as build_host_plan_paged (page_size 1 = row addressing,
+// last_page_len may then be NULL).
+int build_host_plan_multi(int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* last_page_len, int page_size, bool causal, int num_sms,
+                          const PlanOptions& opt, HostPlan* out);
 void free_host_plan(HostPlan* p);
 
 // Device-side view of a plan, passed to the kernels by value.
@@ -95,6 +109,7 @@ struct DecodeArgs {
   float sm_scale;
   const int32_t* kv_last_page_len = nullptr;  // [B], tokens used in each last page (page_size > 1)
   int page_size = 1;                          // tokens per page; 1 = every kv_indices entry is a row
+  const int32_t* qo_indptr = nullptr;         // [B+1] query rows per sequence (multi-token plans)
 };
 
 #ifdef __CUDACC__
@@ -112,6 +127,11 @@ __device__ __forceinline__ int64_t device_seq_tokens(const DecodeArgs& a, int b)
   const int last = a.kv_last_page_len[b];
   if (last < 1 || last > a.page_size) return -1;
   return (pages - 1) * a.page_size + last;
+}
+// The item's query row agrees with the device qo_indptr (always, for
+// single-token calls, which pass none).
+__device__ __forceinline__ bool item_query_ok(const DecodeArgs& a, const WorkItem& w) {
+  return a.qo_indptr == nullptr || (int64_t)a.qo_indptr[w.b] + w.q_tok == w.q_row;
 }
 // kv_indices position (relative to the sequence's first entry) of token t.
 template <bool kPaged>

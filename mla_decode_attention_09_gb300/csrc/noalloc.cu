@@ -128,7 +128,7 @@ int plan_fixed(int batch, const int32_t* ip, int num_sms, FixedPlan* fp) {
     while (cta < fp->n_ctas - 1 && fp->cuts[cta + 1] <= S) ++cta;
     if (S == E) {
       if (n_items >= kMaxItems) return MLA_ERR_NOALLOC_LIMIT;
-      fp->items[n_items++] = WorkItem{b, 0, 0, -1, 0, {0, 0, 0}};
+      fp->items[n_items++] = WorkItem{b, 0, 0, -1, 0, b, 0, 0};
       fp->indptr[cta + 1]++;
       continue;
     }
@@ -136,7 +136,7 @@ int plan_fixed(int batch, const int32_t* ip, int num_sms, FixedPlan* fp) {
       const int64_t a = std::max(S, fp->cuts[cta]), e = std::min(E, fp->cuts[cta + 1]);
       if (e > a) {
         if (n_items >= kMaxItems) return MLA_ERR_NOALLOC_LIMIT;
-        fp->items[n_items++] = WorkItem{b, (int32_t)(a - S), (int32_t)(e - S), -1, (int32_t)(E - S), {0, 0, 0}};
+        fp->items[n_items++] = WorkItem{b, (int32_t)(a - S), (int32_t)(e - S), -1, (int32_t)(E - S), b, 0, 0};
         fp->indptr[cta + 1]++;
       }
       if (E <= fp->cuts[cta + 1] || cta == fp->n_ctas - 1) break;

@@ -48,22 +48,36 @@ namespace {
 
 // The planner proper, on the sequences' token counts laid end to end:
 // tok[b] is the first token of sequence b in that concatenation, tok[batch]
-// the total.
-int plan_tokens(int batch, const std::vector<int64_t>& tok, int num_sms, const PlanOptions& opt, HostPlan* out) {
+// the total; qo[b] is the first query row of sequence b, qo[batch] the number
+// of query rows (single-token plans: qo[b] = b).
+int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<int64_t>& qo, bool causal, int num_sms,
+                const PlanOptions& opt, HostPlan* out) {
   const int64_t total = tok[(size_t)batch];
   out->total_rows = total;
+  auto seq_len = [&](int b) { return tok[(size_t)b + 1] - tok[(size_t)b]; };
+  auto n_queries = [&](int b) { return qo[(size_t)b + 1] - qo[(size_t)b]; };
+  // KV tokens query token j of sequence b sees (its causal prefix, or all)
+  auto visible = [&](int b, int64_t j) {
+    const int64_t L = seq_len(b);
+    const int64_t n = causal ? L - n_queries(b) + j + 1 : L;
+    return std::min<int64_t>(std::max<int64_t>(n, 0), L);
+  };
 
   // Work is counted in granules: sequence b is ceil(L_b / G) granules of G
-  // rows (its last one may be shorter). The granules of all sequences, laid
-  // end to end, are divided evenly among the ranges, so every range gets the
-  // same number of granules to within one and every cut falls on a multiple of
-  // G rows from its sequence's start. With G equal to the kernels' tile height
-  // the ranges hold the same number of tiles to within one.
+  // rows (its last one may be shorter), each weighing the number of query
+  // tokens that read it. The weighted granules of all sequences, laid end to
+  // end, are divided evenly among the ranges, so every range gets the same
+  // weight to within one query token's granule and every cut falls on a
+  // multiple of G rows from its sequence's start. With one query token per
+  // sequence and G equal to the kernels' tile height, the ranges hold the same
+  // number of tiles to within one. A range reads each of its KV rows from HBM
+  // once: the query tokens of one sequence are processed back to back on the
+  // same rows, which the later ones find in L2.
   const int64_t G = opt.granularity;
   const int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
   std::vector<int64_t> gstart((size_t)batch + 1, 0);
   for (int b = 0; b < batch; ++b)
-    gstart[(size_t)b + 1] = gstart[(size_t)b] + (tok[(size_t)b + 1] - tok[(size_t)b] + G - 1) / G;
+    gstart[(size_t)b + 1] = gstart[(size_t)b] + (seq_len(b) + G - 1) / G * n_queries(b);
   const int64_t U = gstart[(size_t)batch];
   int64_t target = U > 0 ? (U + max_ctas - 1) / max_ctas : 1;
   target = std::max<int64_t>(target, (opt.min_rows_per_split + G - 1) / G);
@@ -73,14 +87,14 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, int num_sms, const P
   cuts[(size_t)n_ranges] = total;
   for (int64_t k = 1; k < n_ranges; ++k) {
     const int64_t g = U * k / n_ranges;
-    // sequence holding granule g: last b with gstart[b] <= g (it has granules since g < U)
+    // sequence holding weighted granule g: last b with gstart[b] <= g (it has weight since g < U)
     int lo = 0, hi = batch - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) / 2;
       if (gstart[(size_t)mid] <= g) lo = mid; else hi = mid - 1;
     }
-    const int64_t S = tok[(size_t)lo], L = tok[(size_t)lo + 1] - S;
-    cuts[(size_t)k] = S + std::min<int64_t>((g - gstart[(size_t)lo]) * G, L);
+    const int64_t S = tok[(size_t)lo], L = seq_len(lo);
+    cuts[(size_t)k] = S + std::min<int64_t>((g - gstart[(size_t)lo]) / n_queries(lo) * G, L);
   }
   std::vector<std::pair<int64_t, int64_t>> ranges;  // non-empty CTA row ranges, in order
   for (int64_t k = 0; k < n_ranges; ++k)
@@ -89,22 +103,26 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, int num_sms, const P
 
   std::vector<WorkItem> items;
   std::vector<int32_t> cta_of_item;
-  items.reserve((size_t)batch + ranges.size() * 2);
+  items.reserve((size_t)qo[(size_t)batch] + ranges.size() * 2);
   size_t cta = 0;
   const size_t last = ranges.size() - 1;
+  auto push = [&](int b, int64_t t0, int64_t t1, int64_t j) {
+    items.push_back(WorkItem{b, (int32_t)t0, (int32_t)t1, -1, (int32_t)seq_len(b), (int32_t)(qo[(size_t)b] + j),
+                             (int32_t)j, 0});
+    cta_of_item.push_back((int32_t)cta);
+  };
   for (int b = 0; b < batch; ++b) {
-    const int64_t S = tok[(size_t)b], E = tok[(size_t)b + 1];
+    const int64_t S = tok[(size_t)b], E = tok[(size_t)b + 1], q_b = n_queries(b);
     while (cta < last && ranges[cta].second <= S) ++cta;
-    if (S == E) {  // empty sequence: a zero-row item that writes zeros
-      items.push_back(WorkItem{b, 0, 0, -1, 0, {0, 0, 0}});
-      cta_of_item.push_back((int32_t)cta);
-      continue;
-    }
+    // query tokens that see no KV token write zeros (a zero-row item)
+    for (int64_t j = 0; j < q_b; ++j)
+      if (visible(b, j) == 0) push(b, 0, 0, j);
+    if (S == E || q_b == 0) continue;
     while (true) {
-      const int64_t a = std::max(S, ranges[cta].first), e = std::min(E, ranges[cta].second);
-      if (e > a) {
-        items.push_back(WorkItem{b, (int32_t)(a - S), (int32_t)(e - S), -1, (int32_t)(E - S), {0, 0, 0}});
-        cta_of_item.push_back((int32_t)cta);
+      const int64_t a = std::max(S, ranges[cta].first) - S, e = std::min(E, ranges[cta].second) - S;
+      for (int64_t j = 0; j < q_b; ++j) {  // the query tokens of this row range, back to back
+        const int64_t ej = std::min(e, visible(b, j));
+        if (ej > a) push(b, a, ej, j);
       }
       if (E <= ranges[cta].second || cta == last) break;
       ++cta;
@@ -112,18 +130,21 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, int num_sms, const P
   }
   const int64_t used_ctas = (int64_t)ranges.size();
 
-  // Partial slots for sequences cut into several items (their items are adjacent).
+  // Partial slots for query rows cut into several items, consecutive per row, rows in order.
+  const size_t n_rows = (size_t)qo[(size_t)batch];
+  std::vector<int32_t> count(n_rows, 0), next(n_rows, 0);
+  for (const WorkItem& w : items) count[(size_t)w.q_row]++;
   std::vector<ReduceEntry> reduce;
   int slot = 0;
-  for (size_t i = 0; i < items.size();) {
-    size_t j = i + 1;
-    while (j < items.size() && items[j].b == items[i].b) ++j;
-    if (j - i > 1) {
-      reduce.push_back(ReduceEntry{items[i].b, slot, (int32_t)(j - i), 0});
-      for (size_t k = i; k < j; ++k) items[k].slot = slot++;
+  for (size_t r = 0; r < n_rows; ++r) {
+    if (count[r] > 1) {
+      reduce.push_back(ReduceEntry{(int32_t)r, slot, count[r], 0});
+      next[r] = slot;
+      slot += count[r];
     }
-    i = j;
   }
+  for (WorkItem& w : items)
+    if (count[(size_t)w.q_row] > 1) w.slot = next[(size_t)w.q_row]++;
 
   // Items are already grouped by CTA in increasing order: CSR offsets.
   std::vector<int32_t> indptr((size_t)used_ctas + 1, 0);
@@ -154,6 +175,31 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, int num_sms, const P
   return MLA_OK;
 }
 
+// One query row per sequence.
+std::vector<int64_t> single_queries(int batch) {
+  std::vector<int64_t> qo((size_t)batch + 1);
+  for (int b = 0; b <= batch; ++b) qo[(size_t)b] = b;
+  return qo;
+}
+
+// Token offsets of the paged layout: (pages - 1) * page_size + last page length per sequence.
+int paged_tokens(int batch, const int32_t* kv_indptr, const int32_t* last_page_len, int page_size,
+                 std::vector<int64_t>* tok) {
+  tok->assign((size_t)batch + 1, 0);
+  for (int b = 0; b < batch; ++b) {
+    const int64_t pages = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+    int64_t n = 0;
+    if (pages > 0) {
+      const int64_t last = page_size > 1 ? (int64_t)last_page_len[b] : 1;
+      if (last < 1 || last > page_size) return MLA_ERR_INDPTR;
+      n = (pages - 1) * page_size + last;
+      if (n > INT32_MAX) return MLA_ERR_INDPTR;  // token offsets inside a sequence are 32-bit
+    }
+    (*tok)[(size_t)b + 1] = (*tok)[(size_t)b] + n;
+  }
+  return MLA_OK;
+}
+
 int check_common(int batch, const int32_t* kv_indptr, int num_sms, const PlanOptions& opt, HostPlan* out) {
   if (batch < 0 || num_sms <= 0 || !out || (batch > 0 && !kv_indptr)) return MLA_ERR_ARG;
   if (opt.granularity <= 0 || opt.min_rows_per_split <= 0 || opt.ctas_per_sm <= 0) return MLA_ERR_ARG;
@@ -172,28 +218,36 @@ int build_host_plan(int batch, const int32_t* kv_indptr, int num_sms, const Plan
   if (rc != MLA_OK) return rc;
   std::vector<int64_t> tok((size_t)batch + 1, 0);
   for (int b = 1; b <= batch; ++b) tok[(size_t)b] = kv_indptr[b];
-  return plan_tokens(batch, tok, num_sms, opt, out);
+  return plan_tokens(batch, tok, single_queries(batch), false, num_sms, opt, out);
 }
 
 int build_host_plan_paged(int batch, const int32_t* kv_indptr, const int32_t* last_page_len, int page_size,
                           int num_sms, const PlanOptions& opt, HostPlan* out) {
   if (page_size < 1 || (batch > 0 && page_size > 1 && !last_page_len)) return MLA_ERR_ARG;
-  const int rc = check_common(batch, kv_indptr, num_sms, opt, out);
+  int rc = check_common(batch, kv_indptr, num_sms, opt, out);
   if (rc != MLA_OK) return rc;
-  // Tokens of sequence b: (pages - 1) * page_size + last page length (no pages: none).
-  std::vector<int64_t> tok((size_t)batch + 1, 0);
+  std::vector<int64_t> tok;
+  rc = paged_tokens(batch, kv_indptr, last_page_len, page_size, &tok);
+  if (rc != MLA_OK) return rc;
+  return plan_tokens(batch, tok, single_queries(batch), false, num_sms, opt, out);
+}
+
+int build_host_plan_multi(int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* last_page_len, int page_size, bool causal, int num_sms,
+                          const PlanOptions& opt, HostPlan* out) {
+  if (page_size < 1 || (batch > 0 && (!qo_indptr || (page_size > 1 && !last_page_len)))) return MLA_ERR_ARG;
+  int rc = check_common(batch, kv_indptr, num_sms, opt, out);
+  if (rc != MLA_OK) return rc;
+  if (batch > 0 && qo_indptr[0] != 0) return MLA_ERR_INDPTR;
+  std::vector<int64_t> qo((size_t)batch + 1, 0);
   for (int b = 0; b < batch; ++b) {
-    const int64_t pages = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
-    int64_t n = 0;
-    if (pages > 0) {
-      const int64_t last = page_size > 1 ? (int64_t)last_page_len[b] : 1;
-      if (last < 1 || last > page_size) return MLA_ERR_INDPTR;
-      n = (pages - 1) * page_size + last;
-      if (n > INT32_MAX) return MLA_ERR_INDPTR;  // token offsets inside a sequence are 32-bit
-    }
-    tok[(size_t)b + 1] = tok[(size_t)b] + n;
+    if (qo_indptr[b + 1] < qo_indptr[b]) return MLA_ERR_INDPTR;
+    qo[(size_t)b + 1] = qo_indptr[b + 1];
   }
-  return plan_tokens(batch, tok, num_sms, opt, out);
+  std::vector<int64_t> tok;
+  rc = paged_tokens(batch, kv_indptr, last_page_len, page_size, &tok);
+  if (rc != MLA_OK) return rc;
+  return plan_tokens(batch, tok, qo, causal, num_sms, opt, out);
 }
 
 }  // namespace mla

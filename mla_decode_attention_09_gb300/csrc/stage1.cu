@@ -102,7 +102,7 @@ __device__ __forceinline__ void record_error(int* err, int code) { atomicCAS(err
 
 template <bool kPaged>
 __device__ __forceinline__ bool item_has_tiles(const WorkItem& w, const DecodeArgs& a) {
-  return w.t_end > w.t_begin && device_seq_tokens<kPaged>(a, w.b) == w.seq_len;
+  return w.t_end > w.t_begin && device_seq_tokens<kPaged>(a, w.b) == w.seq_len && item_query_ok(a, w);
 }
 
 // Position in a CTA's stream of tiles.
@@ -299,12 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int it = item_begin; it < item_end; ++it) {
     const WorkItem w = p.items[it];
-    if (device_seq_tokens<kPaged>(a, w.b) != w.seq_len) {
+    if (device_seq_tokens<kPaged>(a, w.b) != w.seq_len || !item_query_ok(a, w)) {
       if (tid == 0) record_error(p.err, MLA_ERR_PLAN_MISMATCH);
       continue;  // skipped by the copy cursor as well
     }
     const int n_rows = w.t_end - w.t_begin;
-    if (n_rows > 0) load_q<MODE>(qa, q, w.b, g, c);
+    if (n_rows > 0) load_q<MODE>(qa, q, w.q_row, g, c);
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     m_run[0] = m_run[1] = -INFINITY;
@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float inv0 = (L0 > 0.f) ? kv_scale / L0 : 0.f;
     const float inv1 = (L1 > 0.f) ? kv_scale / L1 : 0.f;
     if (w.slot < 0) {
-      __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.b * kHeads * kVDim;
+      __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.q_row * kHeads * kVDim;
       if constexpr (MODE == MLA_MODE_BF16) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {

@@ -114,7 +114,7 @@ __device__ __forceinline__ void record_error_u(int* err, int code) { atomicCAS(e
 
 template <bool kPaged>
 __device__ __forceinline__ bool has_tiles(const WorkItem& w, const DecodeArgs& a) {
-  return w.t_end > w.t_begin && device_seq_tokens<kPaged>(a, w.b) == w.seq_len;
+  return w.t_end > w.t_begin && device_seq_tokens<kPaged>(a, w.b) == w.seq_len && item_query_ok(a, w);
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -154,7 +154,7 @@ struct TCur {
   int it, it_end;
   int k;          // index of the current item among the items that have tiles
   int t0, t_begin, t_end;
-  int b;
+  int qrow;       // query / output row of the item
   int64_t base;   // kv_indices offset of the sequence's first entry
   bool done;
 };
@@ -165,7 +165,7 @@ __device__ __forceinline__ void tcur_settle(TCur& c, const DevicePlan& p, const 
     if (has_tiles<kPaged>(w, a)) {
       c.t0 = c.t_begin = w.t_begin;
       c.t_end = w.t_end;
-      c.b = w.b;
+      c.qrow = w.q_row;
       c.base = a.kv_indptr[w.b];
       c.done = false;
       return;
@@ -298,9 +298,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   if (warp == 4 || warp >= 6) {
     // ------------------------------------------------ loaders: KV tiles (+ query staging in warp 4)
     // Every loader walks the same tile stream and takes the same box / row-copy
-    // decision from the same indices. Warp 4 issues the box loads and arrives for
-    // the other two loaders on such tiles, which they skip without waiting; the
-    // row copies of a scattered tile are split among the three loaders.
+    // decision from the same indices. Warp 4 issues the box loads; the row copies
+    // of a scattered tile are split among the three loaders. Every loader waits
+    // for every tile's slot and arrives on every tile's full barrier: the loaders
+    // then stay in lockstep with the slot barriers, whose parity waits cannot
+    // tell a phase from the one two later.
     const bool main_loader = warp == 4;
     const int g = main_loader ? 0 : warp - 5;  // loader rank 0..2
     if (main_loader && lane == 0) {
@@ -394,11 +396,20 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           cont = __all_sync(~0u, cont);
           decided = true;
         }
-        bool ready = !main_loader && cont;  // nothing to copy or wait for
-        if (!ready) {
+        bool ready;
+        if (main_loader) {  // polls: it also stages queries
           ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
           ready = ready && (i < kRopeStages || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
           ready = __shfl_sync(~0u, ready, 0);
+        } else {  // the extra loaders have nothing else to do: a bounded blocking wait
+          const bool w_ok =
+              (i < kLatStages || wait_u(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1, abort_flag)) &&
+              (i < kRopeStages || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag));
+          if (!__all_sync(~0u, w_ok)) {
+            ok = false;
+            break;
+          }
+          ready = true;
         }
         tile_blocked = !ready;
         if (ready) {
@@ -411,7 +422,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
               __syncwarp();
               if (lane < 4) umma::tma_load_2d(lat + lane * kBlk, &tm.lat_tile, lane * 128, y0, fb, pol);
               if (lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
-              if (lane == 0) umma::mbar_arrive_cnt(fb, 32 * (kLoaders - 1));  // for the loaders that skip it
             }
           } else {
             // Row r's index sits in lane (r & 31), slot (r >> 5); loader g copies the
@@ -444,7 +454,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
             if (main_loader && lane == 0) umma::mbar_arrive(fb);
           }
-          if (main_loader || !cont) umma::cp_async_arrive_noinc(fb);
+          umma::cp_async_arrive_noinc(fb);
           // shift the index pipeline: tile i+1's indices are already loaded, request tile i+2's
 #pragma unroll
           for (int j = 0; j < 4; ++j) y0s[j] = y1s[j];
@@ -466,7 +476,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
               q_advance = false;
             }
             if (!qc.done) {
-              load_q(qc.b);
+              load_q(qc.qrow);
               q_loaded = true;
             }
             progress = true;
@@ -587,13 +597,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     bool aborted = false;
     for (int it = item_begin; it < item_end && !aborted; ++it) {
       const WorkItem w = p.items[it];
-      if (device_seq_tokens<kPaged>(a, w.b) != w.seq_len) {
+      if (device_seq_tokens<kPaged>(a, w.b) != w.seq_len || !item_query_ok(a, w)) {
         if (tid == 0) record_error_u(p.err, MLA_ERR_PLAN_MISMATCH);
         continue;
       }
       if (w.t_end <= w.t_begin) {  // empty sequence: zeros
         if (w.slot < 0) {
-          __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.b * kHeads * kVDim;
+          __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.q_row * kHeads * kVDim;
           for (int e = tid; e < kHeads * kVDim / 8; e += 128) reinterpret_cast<uint4*>(ob)[e] = make_uint4(0, 0, 0, 0);
         }
         continue;
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         umma::tmem_ld16(ob + 16u * blk, o);
         const int dcol = 128 * blk + row;
         if (w.slot < 0) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.b * kHeads * kVDim + dcol;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.q_row * kHeads * kVDim + dcol;
 #pragma unroll
           for (int h = 0; h < 16; ++h) out[h * kVDim] = __float2bfloat16_rn(o[h] * inv[h]);
         } else {

@@ -1,0 +1,90 @@
+"""GPU parity of multi-token decode (mla_decode_multi) against the float64 oracle.
+
+Sequence b has q_b query tokens (rows qo_indptr[b] .. of q and out), the last
+q_b tokens of the sequence; causally, query token j sees the first
+L_b - q_b + j + 1 KV tokens (kernelbot amd-mixed-mla submission 690201 "V6c",
+_build_cache: qo_indptr = arange(B+1) * q_seq_len). Tolerances as test_parity.
+"""
+import pytest
+import torch
+
+import mla_inputs as mi
+import oracle
+from test_parity import MODE_IDS, MODES, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_decode_attention_09_gb300 import build
+    build.build()
+    import mla_decode_attention_09_gb300 as m
+    return m
+
+
+def oracle_multi(inp, q, qo, causal):
+    out, _ = oracle.decode_multi(q, inp.kv, qo, inp.kv_indptr, inp.kv_indices, inp.sm_scale, inp.mode, inp.kv_scale,
+                                 causal=causal, kv_last_page_len=inp.kv_last_page_len, page_size=inp.page_size)
+    return out
+
+
+def run_multi(mla, inp, q, qo, causal, num_sms=0, **opts):
+    d = inp.to("cuda")
+    plan = mla.plan_multi(qo, inp.kv_indptr, num_sms, causal=causal, page_size=inp.page_size,
+                          kv_last_page_len_host=inp.kv_last_page_len, num_kv_slots=max(inp.kv.shape[0], 1), **opts)
+    out = torch.full((int(qo[-1]), 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.decode_multi(q.cuda(), d.kv, d.kv_scale_tensor("cuda"), qo.cuda(), d.kv_indptr, d.kv_indices, out, plan=plan,
+                     kv_last_page_len=d.kv_last_page_len, sm_scale=inp.sm_scale, dtype_mode=inp.mode)
+    return out, plan
+
+
+LENGTHS = [300, 10, 0, 1, 1000, 77, 2, 129]
+Q_LENS = [2, 3, 1, 4, 3, 1, 5, 2]
+
+
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+@pytest.mark.parametrize("layout", ["rows", "pages8"])
+@pytest.mark.parametrize("split", ["whole", "split"])
+def test_multi_tokens(mla, mode, k8, causal, layout, split):
+    inp = (mi.make_paged_inputs(LENGTHS, 8, mode, seed=300 + mode, permute=True, extra_pages=3) if layout == "pages8"
+           else mi.make_inputs(LENGTHS, mode, seed=300 + mode, permute=True, extra_slots=11))
+    q, qo = mi.make_query_tokens(Q_LENS, seed=310 + mode, q_std=2.0)
+    opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
+    out, plan = run_multi(mla, inp, q, qo, causal, num_sms=152 if split == "whole" else 6, fp8_kernel=k8, **opts)
+    assert plan.check_error() == 0
+    if split == "split":
+        assert plan.info()["num_split_seqs"] > 0
+    compare(out, oracle_multi(inp, q, qo, causal), mode, f"multi {layout} {split} causal={causal}")
+
+
+def test_multi_query_mismatch_is_reported(mla):
+    inp = mi.make_inputs([64, 40], mi.MODE_BF16, seed=8)
+    q, qo = mi.make_query_tokens([2, 2], seed=9)
+    d = inp.to("cuda")
+    plan = mla.plan_multi(qo, inp.kv_indptr)
+    bad = torch.tensor([0, 1, 4], dtype=torch.int32, device="cuda")  # device disagrees for sequence 1
+    out = torch.zeros((4, 16, 512), dtype=torch.bfloat16, device="cuda")
+    mla.decode_multi(q.cuda(), d.kv, None, bad, d.kv_indptr, d.kv_indices, out, plan=plan, dtype_mode=0)
+    assert plan.check_error() == -3
+    with pytest.raises(mla.MLAError) as e:  # a multi-token plan serves decode_multi only
+        mla.decode(d.q, d.kv, None, d.kv_indptr, d.kv_indices, torch.zeros((2, 16, 512), dtype=torch.bfloat16,
+                                                                         device="cuda"), plan=plan)
+    assert e.value.status == -1
+
+
+# Speculative-decode shape: fp8, B = 64, kv_len = 8192, two query tokens per sequence.
+@pytest.mark.parametrize("k8", [0, 1])
+def test_multi_full_size(mla, k8):
+    inp = mi.make_workload("fp8_b64_l8192")
+    q, qo = mi.make_query_tokens([2] * 64, seed=91)
+    out, plan = run_multi(mla, inp, q, qo, True, fp8_kernel=k8)
+    assert plan.check_error() == 0
+    seqs = [0, 33, 63]
+    rows = [int(qo[b]) + j for b in seqs for j in range(2)]
+    ref_all = oracle_multi(inp, q, qo, True)
+    compare(out[rows], ref_all[rows], mi.MODE_FP8, "multi full size")
+    assert torch.isfinite(out.float()).all()

@@ -155,3 +155,82 @@ def test_paged_plan_rejects_bad_layouts():
     with pytest.raises(mla.MLAError) as e:
         mla.plan_compute_host_paged(np.array([0, 1 << 24], dtype=np.int32), np.array([256], dtype=np.int32), 256, 4)
     assert e.value.status == -10
+
+
+# ---------------------------------------------------------------- several query tokens per sequence
+
+def _visible(L, q, j, causal):
+    return min(max(L - q + j + 1, 0), L) if causal else L
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("num_sms,opts", [(7, dict(min_rows_per_split=16, granularity=16)), (152, {})])
+def test_multi_plan_covers_every_query_token(causal, num_sms, opts):
+    lengths = [300, 10, 0, 1, 4096, 77, 2]
+    q_lens = [2, 3, 1, 4, 3, 0, 5]
+    ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+    ip[1:] = np.cumsum(lengths)
+    qo = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    qo[1:] = np.cumsum(q_lens)
+    r = mla.plan_compute_host_multi(qo, ip, num_sms, causal=causal, **opts)
+    items, wip, red = r["items"], r["work_indptr"], r["reduce"]
+    assert wip[0] == 0 and wip[-1] == len(items)
+    by_row = {}
+    for b, t0, t1, slot, L, q_row, q_tok in items:
+        assert L == lengths[b] and q_row == qo[b] + q_tok and 0 <= q_tok < q_lens[b]
+        by_row.setdefault(int(q_row), []).append((int(t0), int(t1), int(slot)))
+    assert sorted(by_row) == list(range(int(qo[-1])))  # every query row is produced
+    red_map = {int(rw): (int(s0), int(n)) for rw, s0, n in red}
+    for b in range(len(lengths)):
+        for j in range(q_lens[b]):
+            parts = by_row[int(qo[b]) + j]
+            n = _visible(lengths[b], q_lens[b], j, causal)
+            pos = 0
+            for t0, t1, _ in parts:  # contiguous cover of the visible tokens, in order
+                assert t0 == pos
+                pos = t1
+            assert pos == n
+            if len(parts) == 1:
+                assert parts[0][2] == -1 and int(qo[b]) + j not in red_map
+            else:
+                s0, cnt = red_map[int(qo[b]) + j]
+                assert [p[2] for p in parts] == list(range(s0, s0 + cnt))
+    # the query tokens of a sequence's row range sit back to back in one CTA
+    for c in range(r["num_ctas"]):
+        seq_order = [int(items[i, 0]) for i in range(wip[c], wip[c + 1]) if items[i, 2] > items[i, 1]]
+        assert all(seq_order[k] <= seq_order[k + 1] for k in range(len(seq_order) - 1))
+
+
+def test_multi_plan_with_one_query_token_is_the_row_plan():
+    lengths = [700, 5, 0, 4096, 129]
+    ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+    ip[1:] = np.cumsum(lengths)
+    qo = np.arange(len(lengths) + 1, dtype=np.int32)
+    for causal in (True, False):
+        m = mla.plan_compute_host_multi(qo, ip, 9, causal=causal, min_rows_per_split=16, granularity=16)
+        r = mla.plan_compute_host(ip, 9, min_rows_per_split=16, granularity=16)
+        assert np.array_equal(m["items"][:, :5], r["items"])
+        assert np.array_equal(m["work_indptr"], r["work_indptr"]) and np.array_equal(m["reduce"], r["reduce"])
+
+
+def test_multi_plan_balances_weighted_granules():
+    """Every KV granule weighs the number of query tokens of its sequence."""
+    lengths, q_lens = [8192] * 8 + [1024] * 8, [4] * 8 + [1] * 8
+    ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+    ip[1:] = np.cumsum(lengths)
+    qo = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    qo[1:] = np.cumsum(q_lens)
+    r = mla.plan_compute_host_multi(qo, ip, 20, causal=False)
+    items, wip = r["items"], r["work_indptr"]
+    w = [sum(-(-int(items[i, 2] - items[i, 1]) // 128) for i in range(wip[c], wip[c + 1]))
+         for c in range(r["num_ctas"])]
+    assert sum(w) == sum(-(-L // 128) * q for L, q in zip(lengths, q_lens))
+    assert max(w) - min(w) <= 4  # one granule of the heaviest sequence
+
+
+def test_multi_plan_rejects_bad_query_offsets():
+    ip = np.array([0, 10, 20], dtype=np.int32)
+    for bad in ([1, 2, 3], [0, 3, 2]):
+        with pytest.raises(mla.MLAError) as e:
+            mla.plan_compute_host_multi(np.array(bad, dtype=np.int32), ip, 4)
+        assert e.value.status == -10
