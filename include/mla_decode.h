@@ -89,7 +89,7 @@ typedef struct mla_plan_options {
   int64_t num_kv_slots;   /* rows in the KV pool; kv_indices are checked against it in the
                              kernel (out-of-range rows are skipped and MLA_ERR_INDEX recorded).
                              0 = unchecked (the plain mla_decode_plan) */
-  int min_rows_per_split; /* smallest KV chunk the planner cuts (default 256) */
+  int min_rows_per_split; /* smallest KV chunk the planner cuts (default 128, one tile) */
   int granularity;        /* work is balanced in units of this many rows, and chunk boundaries fall on
                              multiples of it from the sequence start (default 128, the fp8 kernel's tile) */
   int ctas_per_sm;        /* persistent CTAs per SM (default 1) */

@@ -59,7 +59,7 @@ struct HostPlan {
 // Resolved planner options (defaults applied).
 struct PlanOptions {
   int64_t num_kv_slots = 0;
-  int min_rows_per_split = 256;
+  int min_rows_per_split = 128;  // one tcgen05 tile: small batches spread over more SMs
   int granularity = 128;  // the tcgen05 kernel's tile height (a multiple of the warp-level kernels' 64)
   int ctas_per_sm = 1;
   int fp8_kernel = 0;  // 0 = tcgen05 / TMA kernel, 1 = warp-level mma.sync kernel

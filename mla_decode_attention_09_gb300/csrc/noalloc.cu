@@ -76,7 +76,7 @@ void setup_device(int dev, DeviceSetup* s) {
 
 // Work list in fixed-capacity arrays (no heap): the same split as the
 // regular planner with its default options (128-row granules balanced across
-// CTAs, chunks of at least 256 rows, one CTA per SM).
+// CTAs, chunks of at least 128 rows, one CTA per SM).
 struct FixedPlan {
   WorkItem items[kMaxItems];
   int32_t indptr[kMaxCtas + 1];
@@ -87,7 +87,7 @@ struct FixedPlan {
 
 // Returns MLA_OK, MLA_ERR_INDPTR, or MLA_ERR_NOALLOC_LIMIT when a fixed capacity is exceeded.
 int plan_fixed(int batch, const int32_t* ip, int num_sms, FixedPlan* fp) {
-  constexpr int64_t G = 128, kMinRows = 256;
+  constexpr int64_t G = 128, kMinRows = 128;
   if (ip[0] != 0) return MLA_ERR_INDPTR;
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) {

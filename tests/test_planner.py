@@ -11,7 +11,7 @@ def _check_plan(lengths, num_sms, **opts):
     r = mla.plan_compute_host(ip, num_sms, **opts)
     items, wip, red = r["items"], r["work_indptr"], r["reduce"]
     G = opts.get("granularity", 128)
-    min_split = opts.get("min_rows_per_split", 256)
+    min_split = opts.get("min_rows_per_split", 128)
     cpsm = opts.get("ctas_per_sm", 1)
     total = int(ip[-1])
     # CTA ranges: CSR over the item list, at most num_sms * ctas_per_sm CTAs
@@ -88,9 +88,9 @@ def test_plan_headline_shapes():
     r = _check_plan([8192] * 64, 152)
     assert r["num_ctas"] == 152
     assert 64 * 2 <= r["num_slots"] <= 64 * 4
-    # B=4 x 1024 bf16: small problem, minimum chunk keeps the split count low
+    # B=4 x 1024 bf16: small problem, one 128-row tile per CTA (the minimum chunk)
     r = _check_plan([1024] * 4, 152)
-    assert r["num_ctas"] == 16
+    assert r["num_ctas"] == 32
     # every CTA gets 26 or 27 of the 4096 tiles of B=64 x 8192
     r = mla.plan_compute_host(np.arange(65, dtype=np.int32) * 8192, 152)
     tiles = [sum(-(-int(t1 - t0) // 128) for _, t0, t1, _, _ in r["items"][r["work_indptr"][c]:r["work_indptr"][c + 1]])
