@@ -95,6 +95,11 @@ typedef struct mla_plan_options {
   int ctas_per_sm;        /* persistent CTAs per SM (default 1) */
   int fp8_kernel;         /* fp8 stage-1 kernel: 0 = 5th-generation tensor cores (tcgen05 + TMA, default),
                              1 = warp-level mma.sync (kept for comparison) */
+  int fp8_issuers;        /* tcgen05 kernel's MMA issue: 2 = two issuing threads (scores, P.V) and two
+                             loader warps, fastest when tiles are runs of consecutive KV rows; 1 = one
+                             issuing thread and three loader warps, fastest when every tile is copied
+                             row by row (scattered rows, small pages). 0 = auto: 1 for page sizes 2..127,
+                             else 2. Results are identical either way. */
 } mla_plan_options;
 
 /* Read-only description of a plan. */

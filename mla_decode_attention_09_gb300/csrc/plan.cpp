@@ -32,6 +32,7 @@ PlanOptions resolve_options(const mla_plan_options* o) {
   if (o->granularity > 0) r.granularity = o->granularity;
   if (o->ctas_per_sm > 0) r.ctas_per_sm = o->ctas_per_sm;
   if (o->fp8_kernel == 1) r.fp8_kernel = 1;
+  if (o->fp8_issuers == 1 || o->fp8_issuers == 2) r.fp8_issuers = o->fp8_issuers;
   return r;
 }
 

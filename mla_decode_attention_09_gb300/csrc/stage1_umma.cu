@@ -22,15 +22,21 @@
 // (submission 690201 "V6c", custom_kernel).
 //
 // Warp roles (256 threads): warps 0-3 softmax and epilogue (warp w reads TMEM
-// lanes 32w..32w+31), warp 4 TMA producer and query staging, warps 6-7 extra
-// loaders for tiles copied row by row (one warp cannot issue those copies fast
-// enough to keep HBM busy; three can come close), warp 5 TMEM
-// allocation and the single MMA-issuing thread. The latent part of a tile
+// lanes 32w..32w+31), warp 4 TMA producer and query staging, warp 5 TMEM
+// allocation. Two instances differ in how the MMAs are issued. With two
+// issuers (kDual), lane 0 of warp 5 issues the score MMAs and lane 0 of warp 6
+// the P.V MMAs, and warp 7 is a second loader for tiles copied row by row.
+// Two in-order chains go faster than one: a single thread issues a small-N
+// tcgen05.mma about every 46-58 cycles, the tensor core takes one every ~39.
+// With one issuer, lane 0 of warp 5 polls both chains and warps 6 and 7 are
+// loaders, which keeps HBM busier when every tile is copied row by row (one
+// warp cannot issue those copies fast enough; three come close). The latent
+// part of a tile
 // (512 B per row, needed until P.V finishes) lives in a 3-slot ring of 64 KB,
 // the rope part (64 B per row, needed only by the scores) in a 2-slot ring of
 // 8 KB, so three tiles can be resident or in flight. S, P and O are double
-// buffered. The producer and the MMA thread poll their barriers and never
-// block one activity on another. The running max per head is updated lazily:
+// buffered. The producer and the single MMA thread poll their barriers and
+// never block one activity on another. The running max per head is updated lazily:
 // O in TMEM is rescaled only when a tile's max exceeds the reference by more
 // than 2^8, so P = 2^(s - m_ref) <= 256 stays inside e4m3's range.
 //
@@ -66,7 +72,6 @@ constexpr int kQBytes = kQLat + 16 * 64;      // + 1 KB rope part
 constexpr int kPBuf = kRowsU * 16;            // 2 KB: P^T [128 tokens][16 heads] e4m3
 constexpr uint32_t kTileTx = kLatStage + kRopeStage;
 constexpr int kThreadsU = 256;
-constexpr int kLoaders = 3;                   // warps 4, 6, 7
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;                 // S^T: 2 buffers x 16 columns
 constexpr uint32_t kColO = 32;                // O^T: 2 buffers x 4 blocks x 16 columns
@@ -88,7 +93,7 @@ enum : int {
   kBQFull = 14,   // query staged (32 arrivals)
   kBQEmpty = 15,  // query consumed (last scores of the item done)
   kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals)
-  kBDrain = 18,   // every MMA of the CTA done
+  kBDrain = 18,   // every MMA of the CTA done (both issuing threads commit)
   kNumBars = 19
 };
 
@@ -239,13 +244,16 @@ struct KvMaps {
   CUtensorMap lat_tile, rope_tile;
 };
 
-template <bool kPaged>
+template <bool kPaged, bool kDual>
 __global__ void __launch_bounds__(kThreadsU, 1)
     mla_stage1_fp8_umma_kernel(const DecodeArgs a, const DevicePlan p, const __grid_constant__ KvMaps tm,
                                const int32_t oob_row) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((int)blockIdx.x >= p.num_ctas) return;
+  // Tiles copied row by row are split among the loader warps: 4 and 7 with
+  // separate score and P.V issuers, 4, 6 and 7 with one issuer.
+  constexpr int kLoaders = kDual ? 2 : 3;
 
   // 1024-aligned base for the swizzle atoms
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     }
     ptx::mbar_init(bar(kBQFull), 32);
     ptx::mbar_init(bar(kBQEmpty), 1);
-    ptx::mbar_init(bar(kBDrain), 1);
+    ptx::mbar_init(bar(kBDrain), kDual ? 2 : 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -295,7 +303,44 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const float kv_scale = __ldg(a.kv_scale);
   const float score_log2 = a.sm_scale * kv_scale * kLog2eU;
 
-  if (warp == 4 || warp >= 6) {
+  // MMA issue of one tile (one thread): scores, and P.V
+  auto issue_qk = [&](const TCur& c, int i) {
+    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
+    const uint32_t d = tmem + kColS + 16u * (uint32_t)(i & 1);
+    umma::fence_after_sync();
+    // row-copied tile: order the cp.async (generic proxy) writes before the tensor core reads them
+    if (row_copy[i % kLatStages]) umma::fence_proxy_async_smem();
+#pragma unroll
+    for (int st = 0; st < 16; ++st) {
+      const uint32_t kb = st >> 2, ko = (st & 3) * 32;
+      umma::mma_f8f6f4(d, umma::smem_desc(lat + kb * kBlk + ko, 16, 1024, umma::kLayoutSw128),
+                       umma::smem_desc(q_addr + kb * 2048 + ko, 16, 1024, umma::kLayoutSw128), kIdescQK, st > 0);
+    }
+#pragma unroll
+    for (int st = 0; st < 2; ++st)
+      umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
+                       umma::smem_desc(q_addr + kQLat + st * 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
+    umma::commit(bar(kBSFull + (i & 1)));
+    umma::commit(bar(kBREmpty + (i & 1)));
+    if (c.t0 + kRowsU >= c.t_end) umma::commit(bar(kBQEmpty));
+  };
+  auto issue_pv = [&](const TCur& d, int i) {
+    const bool first = d.t0 == d.t_begin;
+    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = p_addr + (i & 1) * kPBuf;
+    const uint32_t ob = tmem + kColO + 64u * (uint32_t)(d.k & 1);
+    umma::fence_after_sync();
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        umma::mma_f8f6f4(ob + 16u * blk, umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
+                         umma::smem_desc(p0 + j * 512, 128, 256, umma::kLayoutNone), kIdescPV,
+                         (first && j == 0) ? 0u : 1u);
+    umma::commit(bar(kBPEmpty + (i & 1)));
+    umma::commit(bar(kBLEmpty + i % kLatStages));
+  };
+
+  if (warp == 4 || warp == 7 || (!kDual && warp == 6)) {
     // ------------------------------------------------ loaders: KV tiles (+ query staging in warp 4)
     // Every loader walks the same tile stream and takes the same box / row-copy
     // decision from the same indices. Warp 4 issues the box loads; the row copies
@@ -304,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // then stay in lockstep with the slot barriers, whose parity waits cannot
     // tell a phase from the one two later.
     const bool main_loader = warp == 4;
-    const int g = main_loader ? 0 : warp - 5;  // loader rank 0..2
+    const int g = main_loader ? 0 : (warp == 7 ? kLoaders - 1 : 1);  // loader rank
     if (main_loader && lane == 0) {
       umma::tma_prefetch_desc(&tm.lat_tile);
       umma::tma_prefetch_desc(&tm.rope_tile);
@@ -507,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       if (ptx::mbar_try_wait(b_, par)) continue;
       (void)ptx::mbar_wait_bounded(b_, par, kDrainLimitNsU);
     }
-  } else if (warp == 5) {
+  } else if (warp == 5 && !kDual) {
     // ------------------------------------------------ MMA issue (one thread)
     // P.V of tile j needs the softmax's P; scores of tile j need the tile's
     // data (and, for an item's first tile, its query). Neither waits on the
@@ -515,41 +560,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // of tile j are allowed once P.V of tile j-2 is issued (two S buffers).
     if (lane == 0) {
       bool ok = true;
-      auto issue_qk = [&](const TCur& c, int i) {
-        const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
-        const uint32_t d = tmem + kColS + 16u * (uint32_t)(i & 1);
-        umma::fence_after_sync();
-        // row-copied tile: order the cp.async (generic proxy) writes before the tensor core reads them
-        if (row_copy[i % kLatStages]) umma::fence_proxy_async_smem();
-#pragma unroll
-        for (int st = 0; st < 16; ++st) {
-          const uint32_t kb = st >> 2, ko = (st & 3) * 32;
-          umma::mma_f8f6f4(d, umma::smem_desc(lat + kb * kBlk + ko, 16, 1024, umma::kLayoutSw128),
-                           umma::smem_desc(q_addr + kb * 2048 + ko, 16, 1024, umma::kLayoutSw128), kIdescQK, st > 0);
-        }
-#pragma unroll
-        for (int st = 0; st < 2; ++st)
-          umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
-                           umma::smem_desc(q_addr + kQLat + st * 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
-        umma::commit(bar(kBSFull + (i & 1)));
-        umma::commit(bar(kBREmpty + (i & 1)));
-        if (c.t0 + kRowsU >= c.t_end) umma::commit(bar(kBQEmpty));
-      };
-      auto issue_pv = [&](const TCur& d, int i) {
-        const bool first = d.t0 == d.t_begin;
-        const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = p_addr + (i & 1) * kPBuf;
-        const uint32_t ob = tmem + kColO + 64u * (uint32_t)(d.k & 1);
-        umma::fence_after_sync();
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            umma::mma_f8f6f4(ob + 16u * blk, umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
-                             umma::smem_desc(p0 + j * 512, 128, 256, umma::kLayoutNone), kIdescPV,
-                             (first && j == 0) ? 0u : 1u);
-        umma::commit(bar(kBPEmpty + (i & 1)));
-        umma::commit(bar(kBLEmpty + i % kLatStages));
-      };
       TCur c, d;  // c: next scores tile, d: next P.V tile
       tcur_init<kPaged>(c, item_begin, item_end, p, a);
       d = c;
@@ -587,6 +597,52 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       // every MMA issued by this thread completes before TMEM is released
       umma::commit(bar(kBDrain));
       (void)ptx::mbar_wait_bounded(bar(kBDrain), 0, kDrainLimitNsU);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ score MMAs (one thread)
+    // Scores of tile j need the item's query (first tile), the tile's data, and
+    // the S buffer: the softmax of tile j - 2 has read it (its P is written).
+    if (lane == 0) {
+      bool ok = true;
+      TCur c;
+      tcur_init<kPaged>(c, item_begin, item_end, p, a);
+      int nq = 0;
+      while (!c.done) {
+        ok = (c.t0 != c.t_begin || wait_u(bar(kBQFull), c.k & 1, abort_flag)) &&
+             wait_u(bar(kBFull + nq % kLatStages), (nq / kLatStages) & 1, abort_flag) &&
+             (nq < 2 || wait_u(bar(kBPFull + (nq & 1)), ((nq - 2) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        issue_qk(c, nq);
+        ++nq;
+        tcur_next<kPaged>(c, p, a);
+      }
+      if (!ok) record_error_u(p.err, MLA_ERR_TIMEOUT);
+      // every MMA of both issuing threads completes before TMEM is released
+      umma::commit(bar(kBDrain));
+      (void)ptx::mbar_wait_bounded(bar(kBDrain), 0, kDrainLimitNsU);
+    }
+    __syncwarp();
+  } else if (warp == 6) {  // kDual
+    // ------------------------------------------------ P.V MMAs (one thread)
+    // P.V of tile j needs the softmax's P, and for an item's first tile the O
+    // buffer, freed by the epilogue of the item two before.
+    if (lane == 0) {
+      bool ok = true;
+      TCur d;
+      tcur_init<kPaged>(d, item_begin, item_end, p, a);
+      int npv = 0;
+      while (!d.done) {
+        const bool first = d.t0 == d.t_begin;
+        ok = (!first || d.k < 2 || wait_u(bar(kBOEmpty + (d.k & 1)), ((d.k >> 1) - 1) & 1, abort_flag)) &&
+             wait_u(bar(kBPFull + (npv & 1)), (npv >> 1) & 1, abort_flag);
+        if (!ok) break;
+        issue_pv(d, npv);
+        ++npv;
+        tcur_next<kPaged>(d, p, a);
+      }
+      if (!ok) record_error_u(p.err, MLA_ERR_TIMEOUT);
+      umma::commit(bar(kBDrain));
     }
     __syncwarp();
   } else {
@@ -806,11 +862,12 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(mla_stage1_fp8_umma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SU::kAlloc);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mla_stage1_fp8_umma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SU::kAlloc);
+    void* const kernels[4] = {reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<false, false>),
+                              reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<false, true>),
+                              reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<true, false>),
+                              reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<true, true>)};
+    for (void* k : kernels)
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SU::kAlloc);
     if (e != cudaSuccess) return (int)e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
@@ -836,8 +893,11 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.page_size > 1) return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<true>, a, p, maps, (int32_t)rows);
-  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<false>, a, p, maps, (int32_t)rows);
+  const bool paged = a.page_size > 1, dual = p.dual_issue != 0;
+  if (paged && dual) return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<true, true>, a, p, maps, (int32_t)rows);
+  if (paged) return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<true, false>, a, p, maps, (int32_t)rows);
+  if (dual) return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<false, true>, a, p, maps, (int32_t)rows);
+  return (int)cudaLaunchKernelEx(&cfg, mla_stage1_fp8_umma_kernel<false, false>, a, p, maps, (int32_t)rows);
 }
 
 }  // namespace mla

@@ -10,7 +10,7 @@ import torch
 
 import mla_inputs as mi
 import oracle
-from test_parity import MODE_IDS, MODES, compare
+from test_parity import FP8_KERNEL_IDS, FP8_KERNELS, MODE_IDS, MODES, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def test_multi_tokens(mla, mode, k8, causal, layout, split):
            else mi.make_inputs(LENGTHS, mode, seed=300 + mode, permute=True, extra_slots=11))
     q, qo = mi.make_query_tokens(Q_LENS, seed=310 + mode, q_std=2.0)
     opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
-    out, plan = run_multi(mla, inp, q, qo, causal, num_sms=152 if split == "whole" else 6, fp8_kernel=k8, **opts)
+    out, plan = run_multi(mla, inp, q, qo, causal, num_sms=152 if split == "whole" else 6, **k8, **opts)
     assert plan.check_error() == 0
     if split == "split":
         assert plan.info()["num_split_seqs"] > 0
@@ -77,11 +77,11 @@ def test_multi_query_mismatch_is_reported(mla):
 
 
 # Speculative-decode shape: fp8, B = 64, kv_len = 8192, two query tokens per sequence.
-@pytest.mark.parametrize("k8", [0, 1])
+@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
 def test_multi_full_size(mla, k8):
     inp = mi.make_workload("fp8_b64_l8192")
     q, qo = mi.make_query_tokens([2] * 64, seed=91)
-    out, plan = run_multi(mla, inp, q, qo, True, fp8_kernel=k8)
+    out, plan = run_multi(mla, inp, q, qo, True, **k8)
     assert plan.check_error() == 0
     seqs = [0, 33, 63]
     rows = [int(qo[b]) + j for b in seqs for j in range(2)]

@@ -11,7 +11,7 @@ import torch
 
 import mla_inputs as mi
 import oracle
-from test_parity import MODE_IDS, MODES, compare
+from test_parity import FP8_KERNEL_IDS, FP8_KERNELS, MODE_IDS, MODES, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ LENGTHS = [1, 15, 17, 63, 64, 65, 1000, 0, 129, 2, 300]
 @pytest.mark.parametrize("order", ["contiguous", "shuffled"])
 def test_paged_lengths(mla, mode, k8, ps, order):
     inp = mi.make_paged_inputs(LENGTHS, ps, mode, seed=200 + ps + mode, permute=order == "shuffled", extra_pages=5)
-    out, plan = run_paged(mla, inp, num_sms=7, min_rows_per_split=16, granularity=16, fp8_kernel=k8)
+    out, plan = run_paged(mla, inp, num_sms=7, min_rows_per_split=16, granularity=16, **k8)
     assert plan.check_error() == 0
     assert plan.info()["num_split_seqs"] > 0
     compare(out, oracle_paged(inp), mode, f"paged ps={ps} {order}")
@@ -59,16 +59,16 @@ def test_paged_lengths(mla, mode, k8, ps, order):
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_paged_whole_sequences_default_plan(mla, mode, k8):
     inp = mi.make_paged_inputs([3000, 1, 257, 4096], 8, mode, seed=31, permute=True)
-    out, plan = run_paged(mla, inp, fp8_kernel=k8)
+    out, plan = run_paged(mla, inp, **k8)
     assert plan.check_error() == 0
     compare(out, oracle_paged(inp), mode, "paged default plan")
 
 
-@pytest.mark.parametrize("k8", [0, 1])
+@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
 def test_paged_last_page_mismatch_is_reported(mla, k8):
     inp = mi.make_paged_inputs([40, 33], 8, mi.MODE_FP8, seed=3)
     d = inp.to("cuda")
-    plan = mla.plan_paged(inp.kv_indptr, inp.kv_last_page_len, 8, fp8_kernel=k8)
+    plan = mla.plan_paged(inp.kv_indptr, inp.kv_last_page_len, 8, **k8)
     lp = d.kv_last_page_len.clone()
     lp[1] = 2  # device disagrees with the plan for sequence 1
     out = torch.zeros((2, 16, 512), dtype=torch.bfloat16, device="cuda")
@@ -79,12 +79,12 @@ def test_paged_last_page_mismatch_is_reported(mla, k8):
     compare(out[:1], oracle_paged(inp, seq_ids=[0]), mi.MODE_FP8, "paged mismatch, other sequence")
 
 
-@pytest.mark.parametrize("k8", [0, 1])
+@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
 def test_paged_out_of_range_page_is_reported(mla, k8):
     inp = mi.make_paged_inputs([40, 33], 8, mi.MODE_FP8, seed=4)
     inp.kv_indices[2] = inp.kv.shape[0] // 8  # one past the last page
     d = inp.to("cuda")
-    plan = mla.plan_paged(inp.kv_indptr, inp.kv_last_page_len, 8, num_kv_slots=inp.kv.shape[0], fp8_kernel=k8)
+    plan = mla.plan_paged(inp.kv_indptr, inp.kv_last_page_len, 8, num_kv_slots=inp.kv.shape[0], **k8)
     out = torch.zeros((2, 16, 512), dtype=torch.bfloat16, device="cuda")
     mla.decode_paged(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, d.kv_last_page_len, 8, out,
                      sm_scale=inp.sm_scale, dtype_mode=inp.mode, plan=plan)

@@ -27,7 +27,11 @@ def mla():
     return m
 
 
-FP8_KERNELS = [0, 1]  # 0: tcgen05 / TMA kernel (default), 1: warp-level mma.sync kernel
+# fp8 stage-1 kernels: the tcgen05 / TMA kernel (default) in both of its MMA
+# issue instances, and the warp-level mma.sync kernel
+KERNELS = {"tcgen05": {"fp8_issuers": 2}, "tcgen05-1issuer": {"fp8_issuers": 1}, "mma": {"fp8_kernel": 1}}
+FP8_KERNELS = list(KERNELS.values())
+FP8_KERNEL_IDS = list(KERNELS)
 
 
 def run(mla, inp: mi.Inputs, num_sms=0, **opts):
@@ -61,8 +65,8 @@ def oracle_out(inp: mi.Inputs, seq_ids=None):
 ODD = [1, 15, 17, 63, 64, 65, 1000, 0, 129, 2]
 
 
-MODES = [(mi.MODE_BF16, 0), (mi.MODE_FP8, 0), (mi.MODE_FP8, 1), (mi.MODE_A16W8, 0)]
-MODE_IDS = ["bf16", "fp8-tcgen05", "fp8-mma", "a16w8"]
+MODES = [(mi.MODE_BF16, {})] + [(mi.MODE_FP8, k) for k in FP8_KERNELS] + [(mi.MODE_A16W8, {})]
+MODE_IDS = ["bf16"] + [f"fp8-{k}" for k in FP8_KERNEL_IDS] + ["a16w8"]
 
 
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
@@ -70,7 +74,7 @@ MODE_IDS = ["bf16", "fp8-tcgen05", "fp8-mma", "a16w8"]
 def test_odd_lengths(mla, mode, k8, split):
     inp = mi.make_inputs(ODD, mode, seed=100 + mode, permute=True, extra_slots=37)
     opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
-    out, plan = run(mla, inp, num_sms=152 if split == "whole" else 5, fp8_kernel=k8, **opts)
+    out, plan = run(mla, inp, num_sms=152 if split == "whole" else 5, **k8, **opts)
     info = plan.info()
     if split == "split":
         assert info["num_split_seqs"] > 0
@@ -80,7 +84,7 @@ def test_odd_lengths(mla, mode, k8, split):
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_one_long_sequence_many_splits(mla, mode, k8):
     inp = mi.make_inputs([5003], mode, seed=7)
-    out, plan = run(mla, inp, num_sms=152, min_rows_per_split=16, granularity=16, fp8_kernel=k8)
+    out, plan = run(mla, inp, num_sms=152, min_rows_per_split=16, granularity=16, **k8)
     assert plan.info()["num_partial_slots"] > 100
     compare(out, oracle_out(inp), mode, "one long sequence")
 
@@ -89,17 +93,17 @@ def test_one_long_sequence_many_splits(mla, mode, k8):
 def test_peaked_scores(mla, mode, k8):
     # larger query norm -> sharply peaked softmax; exercises the running-max rescale
     inp = mi.make_inputs([300, 1, 77, 2000], mode, seed=9, q_std=6.0)
-    out, _ = run(mla, inp, num_sms=4, min_rows_per_split=16, fp8_kernel=k8)
+    out, _ = run(mla, inp, num_sms=4, min_rows_per_split=16, **k8)
     compare(out, oracle_out(inp), mode, "peaked")
 
 
-@pytest.mark.parametrize("k8", FP8_KERNELS)
+@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
 def test_fp8_query_cast_saturates(mla, k8):
     # entries beyond +-448 exercise the saturating direct cast of the query
     inp = mi.make_inputs([40, 9], mi.MODE_FP8, seed=13)
     inp.q[0, 3, :50] = 1000.0
     inp.q[1, 5, 100:140] = -600.0
-    out, _ = run(mla, inp, fp8_kernel=k8)
+    out, _ = run(mla, inp, **k8)
     ref = oracle_out(inp)
     compare(out, ref, mi.MODE_FP8, "fp8 saturation")
 
@@ -107,8 +111,8 @@ def test_fp8_query_cast_saturates(mla, k8):
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_stage1_plus_reduce_equals_decode_and_is_deterministic(mla, mode, k8):
     inp = mi.make_inputs([700, 333, 64], mode, seed=21)
-    a, plan = run(mla, inp, num_sms=6, min_rows_per_split=16, fp8_kernel=k8)
-    b, _ = run(mla, inp, num_sms=6, min_rows_per_split=16, fp8_kernel=k8)
+    a, plan = run(mla, inp, num_sms=6, min_rows_per_split=16, **k8)
+    b, _ = run(mla, inp, num_sms=6, min_rows_per_split=16, **k8)
     assert torch.equal(a, b)
     d = inp.to("cuda")
     c = torch.empty_like(a)
@@ -138,12 +142,12 @@ def test_plan_mismatch_is_reported(mla):
     assert plan.check_error() == 0    # cleared after reading
 
 
-@pytest.mark.parametrize("k8", FP8_KERNELS)
+@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
 def test_out_of_range_index_is_reported(mla, k8):
     inp = mi.make_inputs([30, 20], mi.MODE_FP8, seed=4)
     inp.kv_indices[7] = inp.kv.shape[0] + 5
     d = inp.to("cuda")
-    plan = mla.plan(inp.kv_indptr, 0, num_kv_slots=inp.kv.shape[0], fp8_kernel=k8)
+    plan = mla.plan(inp.kv_indptr, 0, num_kv_slots=inp.kv.shape[0], **k8)
     out = torch.zeros((2, 16, 512), dtype=torch.bfloat16, device="cuda")
     mla.decode(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, out, plan=plan)
     assert plan.check_error() == -8   # MLA_ERR_INDEX; the bad row was read as zeros
@@ -177,14 +181,16 @@ SAMPLES = {"bf16_b4_l1024": None, "fp8_b4_l8192": None, "fp8_b64_l1024": [0, 17,
            "a16w8_b64_l8192": [0, 25, 50, 63]}
 
 
-FULL = ([(n, 0) for n in mi.WORKLOADS] + [(n, 1) for n, w in mi.WORKLOADS.items() if w.mode == mi.MODE_FP8]
-        + [(n, 0) for n in mi.EXTRA_WORKLOADS])
+# the default plan (no options) is the launch configuration the benchmark times
+FULL = ([(n, "default") for n in mi.WORKLOADS] + [(n, k) for n, w in mi.WORKLOADS.items() if w.mode == mi.MODE_FP8
+                                                  for k in ("tcgen05-1issuer", "mma")]
+        + [(n, "default") for n in mi.EXTRA_WORKLOADS])
 
 
-@pytest.mark.parametrize("name,k8", FULL, ids=[f"{n}-k{k}" for n, k in FULL])
-def test_full_size_workload(mla, name, k8):
+@pytest.mark.parametrize("name,kernel", FULL, ids=[f"{n}-{k}" for n, k in FULL])
+def test_full_size_workload(mla, name, kernel):
     inp = mi.make_workload(name)
-    out, plan = run(mla, inp, fp8_kernel=k8)   # default plan (k8=0): the launch configuration the benchmark times
+    out, plan = run(mla, inp, **KERNELS.get(kernel, {}))
     ids = SAMPLES[name]
     ref = oracle_out(inp, seq_ids=ids)
     got = out if ids is None else out[torch.tensor(ids, device="cuda")]
