@@ -96,10 +96,9 @@ typedef struct mla_plan_options {
   int fp8_kernel;         /* fp8 stage-1 kernel: 0 = 5th-generation tensor cores (tcgen05 + TMA, default),
                              1 = warp-level mma.sync (kept for comparison) */
   int fp8_issuers;        /* tcgen05 kernel's MMA issue: 2 = two issuing threads (scores, P.V) and two
-                             loader warps, fastest when tiles are runs of consecutive KV rows; 1 = one
-                             issuing thread and three loader warps, fastest when every tile is copied
-                             row by row (scattered rows, small pages). 0 = auto: 1 for page sizes 2..127,
-                             else 2. Results are identical either way. */
+                             loader warps (default); 1 = one issuing thread and three loader warps, a
+                             few per cent faster only when the KV rows of page-size-1 sequences are
+                             scattered one by one. 0 = default. Results are identical either way. */
 } mla_plan_options;
 
 /* Read-only description of a plan. */
@@ -267,7 +266,10 @@ int mla_decode_noalloc(const void* q, const void* kv, const float* kv_scale, con
  * kv_last_page_len[b] tokens (1 <= len <= page_size), every other page holds
  * page_size. Token t is row kv_indices[kv_indptr[b] + t / page_size] *
  * page_size + t % page_size of the buffer. The rows of a last page past its
- * length are never read into the result.
+ * length never reach the result (they may hold anything, NaN codes included),
+ * but the fp8 tensor-core kernel may load them: with pages of 16, 32 or 64
+ * rows it loads whole pages, so every listed page must lie whole inside the
+ * buffer.
  *
  * mla_decode_plan_paged — the planner for that layout.
  *   kv_indptr_host        host int32 [B+1] page offsets (0 first, non-decreasing).

@@ -161,7 +161,7 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   p->dev.num_ctas = h.num_ctas;
   p->dev.n_reduce = h.n_reduce;
   p->dev.fp8_kernel = opt.fp8_kernel;
-  p->dev.dual_issue = mla::dual_issue(opt, l.page_size) ? 1 : 0;
+  p->dev.dual_issue = mla::dual_issue(opt) ? 1 : 0;
   p->zero_row = base + o_zero;
   p->refcount = 1;
   *out = p;

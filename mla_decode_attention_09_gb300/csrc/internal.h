@@ -63,16 +63,13 @@ struct PlanOptions {
   int granularity = 128;  // the tcgen05 kernel's tile height (a multiple of the warp-level kernels' 64)
   int ctas_per_sm = 1;
   int fp8_kernel = 0;  // 0 = tcgen05 / TMA kernel, 1 = warp-level mma.sync kernel
-  int fp8_issuers = 0;  // tcgen05 kernel: 0 auto (by page size), 1 one MMA issuer, 2 two
+  int fp8_issuers = 0;  // tcgen05 kernel: 0 or 2 two MMA-issuing threads, 1 one issuer + three loaders
 };
 
-// Two MMA-issuing threads in the tcgen05 kernel unless the layout makes every
-// tile a row-by-row copy (pages shorter than a tile), where a third loader
-// warp is worth more than a second issuer.
-inline bool dual_issue(const PlanOptions& o, int page_size) {
-  if (o.fp8_issuers != 0) return o.fp8_issuers == 2;
-  return !(page_size > 1 && page_size < 128);
-}
+// Two MMA-issuing threads in the tcgen05 kernel unless asked for one: one
+// issuer frees a warp for a third row loader, which pays only when every
+// tile is copied row by row from rows scattered one by one.
+inline bool dual_issue(const PlanOptions& o) { return o.fp8_issuers != 1; }
 
 PlanOptions resolve_options(const mla_plan_options* o);
 
@@ -106,7 +103,7 @@ struct DevicePlan {
   int num_ctas;
   int n_reduce;
   int fp8_kernel;        // see PlanOptions
-  int dual_issue;        // tcgen05 kernel instance: 1 two MMA issuers, 0 one (see dual_issue())
+  int dual_issue;        // tcgen05 kernel instance: 1 two MMA issuers, 0 one
 };
 
 struct DecodeArgs {

@@ -214,7 +214,7 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const float* kv
   p.num_kv_slots = num_kv_slots > 0 ? num_kv_slots : 0;
   p.num_ctas = fp.n_ctas;
   p.n_reduce = fp.n_reduce;
-  p.dual_issue = 1;  // rows addressed one by one (page size 1)
+  p.dual_issue = 1;
   const DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
   if (launch_stage1(dtype_mode, a, p, base + kZeroOff, stream) != 0) return MLA_ERR_CUDA;
   if (launch_reduce(out, p, stream, true) != 0) return MLA_ERR_CUDA;

@@ -41,12 +41,14 @@
 // than 2^8, so P = 2^(s - m_ref) <= 256 stays inside e4m3's range.
 //
 // A tile whose 128 rows are consecutive in the KV buffer arrives by TMA as
-// five 2-D box loads. Any other tile (rows scattered by kv_indices, or pages
-// shorter than a tile) is copied by the three loader warps with 16-byte
-// cp.async, one 512-byte latent row per instruction, into the same swizzled
-// layout the box loads produce. Rows past the end of an item, and rows whose index is out
-// of range, are read at an out-of-bounds coordinate (TMA) or zero-filled
-// (cp.async).
+// five 2-D box loads. With pages of 16, 32 or 64 rows, a tile that starts
+// on a page boundary arrives as five box loads per page, each box one page
+// high, landing at the page's rows of the tile. Any other tile (rows
+// scattered by kv_indices, or a tile not aligned to pages) is copied by the
+// loader warps with 16-byte cp.async, one 512-byte latent row per
+// instruction, into the same swizzled layout the box loads produce. Rows past
+// the end of an item, and rows whose index is out of range, are read at an
+// out-of-bounds coordinate (TMA) or zero-filled (cp.async).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -241,8 +243,17 @@ __device__ __forceinline__ int q_offset(int h, int d0) {
 }
 
 struct KvMaps {
-  CUtensorMap lat_tile, rope_tile;
+  CUtensorMap lat_tile, rope_tile;  // 128-row boxes
+  CUtensorMap lat_page, rope_page;  // one-page boxes (page sizes 16..64), else unused
 };
+
+// Page sizes whose pages are loaded as one box each: a power of two from 16
+// to 64 (half a tile). Boxes must start on a 1024-byte swizzle atom (8 latent
+// rows); pages of 8 would work too but measured slower than row copies (80
+// small boxes per tile).
+__host__ __device__ constexpr bool page_boxes(int page_size) {
+  return page_size >= 16 && page_size <= 64 && (page_size & (page_size - 1)) == 0;
+}
 
 template <bool kPaged, bool kDual>
 __global__ void __launch_bounds__(kThreadsU, 1)
@@ -353,6 +364,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     if (main_loader && lane == 0) {
       umma::tma_prefetch_desc(&tm.lat_tile);
       umma::tma_prefetch_desc(&tm.rope_tile);
+      if (kPaged && page_boxes(a.page_size)) {
+        umma::tma_prefetch_desc(&tm.lat_page);
+        umma::tma_prefetch_desc(&tm.rope_page);
+      }
     }
     const uint64_t pol = ptx::l2_evict_first_policy();
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
@@ -420,8 +435,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     bool q_loaded = false, q_advance = false;
     int i = 0;
     bool ok = true;
-    bool decided = false, cont = false;  // box / row-copy decision for tile c, taken once
+    bool decided = false, cont = false, runs = false;  // box / page-box / row-copy decision for tile c
     int y0 = oob_row;
+    // page boxes: lane k < nruns loads page k of the tile, whose first KV row is run_y
+    const int run_ps = (kPaged && page_boxes(a.page_size)) ? a.page_size : 0;
+    int nruns = 0, run_y = oob_row;
     IdleClock idle;
     while (!c.done || !qc.done) {
       bool progress = false, tile_blocked = c.done;
@@ -439,6 +457,20 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) cont = cont && (lane + 32 * j >= nv || y0s[j] == y0 + lane + 32 * j);
           cont = __all_sync(~0u, cont);
+          runs = false;
+          if constexpr (kPaged) {
+            if (!cont && run_ps > 0 && c.t0 % run_ps == 0) {
+              // The tile's pages are whole (a page starts every run_ps rows); the
+              // last one may extend past the item, read from the caller's page.
+              const int src = (lane * run_ps) & 31, slot = (lane * run_ps) >> 5;
+              const int v0 = __shfl_sync(~0u, y0s[0], src), v1 = __shfl_sync(~0u, y0s[1], src);
+              const int v2 = __shfl_sync(~0u, y0s[2], src), v3 = __shfl_sync(~0u, y0s[3], src);
+              nruns = (min(nv, kRowsU) + run_ps - 1) / run_ps;  // nv counts the item's rows left
+              run_y = lane >= nruns ? oob_row : slot == 0 ? v0 : slot == 1 ? v1 : slot == 2 ? v2 : v3;
+              // a page with an out-of-range index takes the row-copy path (zeros)
+              runs = __all_sync(~0u, lane >= nruns || run_y != oob_row);
+            }
+          }
           decided = true;
         }
         bool ready;
@@ -460,8 +492,19 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (ready) {
           const uint32_t fb = bar(kBFull + ls);
           const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
-          if (main_loader && lane == 0) row_copy[ls] = cont ? 0 : 1;  // published by the arrivals below
-          if (cont) {
+          if (main_loader && lane == 0) row_copy[ls] = (cont || runs) ? 0 : 1;  // published by the arrivals below
+          if (runs) {
+            if (main_loader) {
+              if (lane == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)(nruns * run_ps * kQkDim));
+              __syncwarp();
+              if (lane < nruns) {
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb)
+                  umma::tma_load_2d(lat + cb * kBlk + lane * run_ps * 128, &tm.lat_page, cb * 128, run_y, fb, pol);
+                umma::tma_load_2d(rope + lane * run_ps * 64, &tm.rope_page, 512, run_y, fb, pol);
+              }
+            }
+          } else if (cont) {
             if (main_loader) {
               if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kTileTx);
               __syncwarp();
@@ -831,7 +874,7 @@ EncodeTiledFn encode_fn() {
 // Two views of the e4m3 KV pool [rows x 576 bytes] as 128-row tiles: the
 // latent part in 128-byte boxes (128-byte swizzle) and the rope part in
 // 64-byte boxes (64-byte swizzle).
-int make_kv_maps(const void* kv, int64_t rows, KvMaps* m) {
+int make_kv_maps(const void* kv, int64_t rows, int page_size, KvMaps* m) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)kQkDim, (cuuint64_t)rows};
@@ -843,9 +886,13 @@ int make_kv_maps(const void* kv, int64_t rows, KvMaps* m) {
     cuuint32_t w, h;
     CUtensorMapSwizzle sw;
   };
-  const View views[2] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
-                         {&m->rope_tile, 64, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_64B}};
+  const View views[4] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
+                         {&m->rope_tile, 64, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_64B},
+                         {&m->lat_page, 128, (cuuint32_t)page_size, CU_TENSOR_MAP_SWIZZLE_128B},
+                         {&m->rope_page, 64, (cuuint32_t)page_size, CU_TENSOR_MAP_SWIZZLE_64B}};
+  *m = KvMaps{};
   for (const View& v : views) {
+    if (v.h != (cuuint32_t)kRowsU && !page_boxes(page_size)) continue;
     const cuuint32_t box[2] = {v.w, v.h};
     if (enc(v.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, v.sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -876,12 +923,15 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
   const int64_t rows = (p.num_kv_slots > 0 && p.num_kv_slots < 0x7fffffff) ? p.num_kv_slots : 0x7fffffff;
   thread_local const void* cached_kv = nullptr;
   thread_local int64_t cached_rows = -1;
+  thread_local int cached_ps = -1;
   thread_local KvMaps maps;
-  if (cached_kv != a.kv || cached_rows != rows) {
-    const int rc = make_kv_maps(a.kv, rows, &maps);
+  if (cached_kv != a.kv || cached_rows != rows || cached_ps != a.page_size) {
+    cached_kv = nullptr;
+    const int rc = make_kv_maps(a.kv, rows, a.page_size, &maps);
     if (rc != 0) return rc;
     cached_kv = a.kv;
     cached_rows = rows;
+    cached_ps = a.page_size;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_ctas);

@@ -46,7 +46,7 @@ LENGTHS = [1, 15, 17, 63, 64, 65, 1000, 0, 129, 2, 300]
 
 
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("ps", [2, 3, 8, 16, 64, 128, 256])
+@pytest.mark.parametrize("ps", [2, 3, 8, 16, 32, 64, 128, 256])
 @pytest.mark.parametrize("order", ["contiguous", "shuffled"])
 def test_paged_lengths(mla, mode, k8, ps, order):
     inp = mi.make_paged_inputs(LENGTHS, ps, mode, seed=200 + ps + mode, permute=order == "shuffled", extra_pages=5)
@@ -62,6 +62,31 @@ def test_paged_whole_sequences_default_plan(mla, mode, k8):
     out, plan = run_paged(mla, inp, **k8)
     assert plan.check_error() == 0
     compare(out, oracle_paged(inp), mode, "paged default plan")
+
+
+@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
+@pytest.mark.parametrize("ps", [8, 16, 32, 64])
+@pytest.mark.parametrize("checked", [True, False])
+def test_paged_unused_rows_of_last_pages_are_ignored(mla, k8, ps, checked):
+    # Pages of 16..64 rows arrive as whole pages, so the rows of a last page past
+    # kv_last_page_len are read too. Poison them with e4m3 NaN codes (0x7f): the
+    # output must not see them. Tails of 1, ps - 1 and a few rows; the default plan
+    # (tiles start on page boundaries), with and without the pool size.
+    inp = mi.make_paged_inputs([3 * ps + 5, 1, 5 * ps - 1, 130, 2 * ps], ps, mi.MODE_FP8, seed=40 + ps,
+                               permute=True, extra_pages=3)
+    for b in range(inp.batch):
+        lo, hi = int(inp.kv_indptr[b]), int(inp.kv_indptr[b + 1])
+        if hi > lo:
+            page, used = int(inp.kv_indices[hi - 1]), int(inp.kv_last_page_len[b])
+            inp.kv[page * ps + used:(page + 1) * ps] = 0x7F
+    d = inp.to("cuda")
+    plan = mla.plan_paged(inp.kv_indptr, inp.kv_last_page_len, ps,
+                          num_kv_slots=inp.kv.shape[0] if checked else 0, **k8)
+    out = torch.full((inp.batch, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.decode_paged(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, d.kv_last_page_len, ps,
+                     out, sm_scale=inp.sm_scale, dtype_mode=inp.mode, plan=plan)
+    assert plan.check_error() == 0
+    compare(out, oracle_paged(inp), mi.MODE_FP8, f"poisoned last pages ps={ps}")
 
 
 @pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
