@@ -327,7 +327,7 @@ int mla_decode_paged(const void* q, const void* kv, const float* kv_scale, const
   if (rc != MLA_OK) return rc;
   mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
   a.kv_last_page_len = l.last;
-  a.page_size = page_size;
+  mla::set_page_size(a, page_size);
   return decode_common(a, dtype_mode, workspace, stream, true);
 }
 
@@ -340,7 +340,7 @@ int mla_decode_multi(const void* q, const void* kv, const float* kv_scale, const
   if (rc != MLA_OK) return rc;
   mla::DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
   a.kv_last_page_len = l.last;
-  a.page_size = page_size;
+  mla::set_page_size(a, page_size);
   a.qo_indptr = qo_indptr;
   return decode_common(a, dtype_mode, workspace, stream, true);
 }

@@ -459,13 +459,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           cont = __all_sync(~0u, cont);
           runs = false;
           if constexpr (kPaged) {
-            if (!cont && run_ps > 0 && c.t0 % run_ps == 0) {
+            if (!cont && run_ps > 0 && (c.t0 & (run_ps - 1)) == 0) {
               // The tile's pages are whole (a page starts every run_ps rows); the
               // last one may extend past the item, read from the caller's page.
               const int src = (lane * run_ps) & 31, slot = (lane * run_ps) >> 5;
               const int v0 = __shfl_sync(~0u, y0s[0], src), v1 = __shfl_sync(~0u, y0s[1], src);
               const int v2 = __shfl_sync(~0u, y0s[2], src), v3 = __shfl_sync(~0u, y0s[3], src);
-              nruns = (min(nv, kRowsU) + run_ps - 1) / run_ps;  // nv counts the item's rows left
+              nruns = (min(nv, kRowsU) + run_ps - 1) >> a.page_shift;  // run_ps = 2^page_shift; nv counts the item's rows left
               run_y = lane >= nruns ? oob_row : slot == 0 ? v0 : slot == 1 ? v1 : slot == 2 ? v2 : v3;
               // a page with an out-of-range index takes the row-copy path (zeros)
               runs = __all_sync(~0u, lane >= nruns || run_y != oob_row);

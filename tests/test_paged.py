@@ -46,7 +46,7 @@ LENGTHS = [1, 15, 17, 63, 64, 65, 1000, 0, 129, 2, 300]
 
 
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("ps", [2, 3, 8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("ps", [2, 3, 8, 16, 24, 32, 64, 128, 256])
 @pytest.mark.parametrize("order", ["contiguous", "shuffled"])
 def test_paged_lengths(mla, mode, k8, ps, order):
     inp = mi.make_paged_inputs(LENGTHS, ps, mode, seed=200 + ps + mode, permute=order == "shuffled", extra_pages=5)
