@@ -307,9 +307,23 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   ptx::griddep_launch_dependents();
   // The launch allows this grid to start while the previous kernel in the
   // stream finishes: everything above touches only this CTA's shared memory and
-  // TMEM. Wait for that kernel's completion before any global memory access.
-  ptx::griddep_wait();
+  // TMEM. The plan's arrays were written when the plan was made and may be
+  // read now; the caller's arrays are read only after that kernel completes.
+  // Meanwhile the first item's plan entry, kv_indptr entry and query are
+  // prefetched into L2 (a prefetch consumes no data).
   const int item_begin = p.work_indptr[blockIdx.x], item_end = p.work_indptr[blockIdx.x + 1];
+  if (warp == 7 && lane == 0 && item_begin < item_end) {
+    const WorkItem w0 = p.items[item_begin];
+    ptx::prefetch_l2(a.kv_indptr + w0.b);
+    ptx::prefetch_l2(a.kv_indptr + w0.b + 1);
+    if (kPaged) ptx::prefetch_l2(a.kv_last_page_len + w0.b);
+    // single-token calls: query row b of the B rows the plan was made for (a
+    // multi-token row is known valid only once qo_indptr has been checked)
+    if (a.qo_indptr == nullptr)
+      umma::bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(a.q) + (int64_t)w0.q_row * kHeads * kQkDim,
+                             kHeads * kQkDim * 2);
+  }
+  ptx::griddep_wait();
 
   const float kv_scale = __ldg(a.kv_scale);
   const float score_log2 = a.sm_scale * kv_scale * kLog2eU;
@@ -420,7 +434,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // c: next tile to load; c1, c2: the two after. qc: item whose query is staged next.
     // Tile loads come first. Loading and casting a query stalls the warp on global
     // loads, so it runs only when no tile can be issued (the ring is full, or every
-    // tile is issued); the first item's query lands while its first tiles are in flight.
+    // tile is issued). The queries of the second and later items are staged here;
+    // the first item's is staged by the softmax warps at the start.
     TCur c, c1, c2, qc;
     tcur_init<kPaged>(c, item_begin, item_end, p, a);
     c1 = c;
@@ -432,7 +447,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     int y0s[4], y1s[4];
     load_rows(c, y0s);
     load_rows(c1, y1s);
-    bool q_loaded = false, q_advance = false;
+    bool q_loaded = false, q_advance = true;  // the first item's query is staged by warps 0-3
     int i = 0;
     bool ok = true;
     bool decided = false, cont = false, runs = false;  // box / page-box / row-copy decision for tile c
@@ -692,6 +707,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // ------------------------------------------------ softmax + epilogue (warps 0-3, thread = token row)
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
     const int row = 32 * warp + lane;
+    {
+      // Query of the first item with tiles, as e4m3 in the staged layout: 128
+      // threads with nine 16-byte loads each, all in flight at once, so it lands
+      // about when the first KV tile does (one loader warp would take several
+      // round trips and hold back the first scores).
+      TCur c0;
+      tcur_init<kPaged>(c0, item_begin, item_end, p, a);
+      if (!c0.done) {
+        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)c0.qrow * kHeads * kQkDim;
+        uint4 raw[9];
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const int ci = tid + 128 * j, h = ci / 72, d0 = (ci % 72) * 8;
+          raw[j] = __ldg(reinterpret_cast<const uint4*>(qb + h * kQkDim + d0));
+        }
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const int ci = tid + 128 * j, h = ci / 72, d0 = (ci % 72) * 8;
+          *reinterpret_cast<uint2*>(smem + SU::kQ + q_offset(h, d0)) =
+              make_uint2(cast4_e4m3(raw[j].x, raw[j].y), cast4_e4m3(raw[j].z, raw[j].w));
+        }
+        umma::fence_proxy_async_smem();
+        ptx::named_bar_sync(1, 128);
+        if (warp == 0) umma::mbar_arrive(bar(kBQFull));  // 32 arrivals complete the phase
+      }
+    }
     int i = 0, k = 0;
     bool aborted = false;
     for (int it = item_begin; it < item_end && !aborted; ++it) {
