@@ -219,6 +219,17 @@ def oracle_sample(w: mi.Workload, inp: mi.Inputs, n_seq: int):
 
 # ---------------------------------------------------------------- our arm
 
+def parse_layout(text: str):
+    """'rows' | 'rows:shuffled' | 'pages:N' | 'pages:N:shuffled' -> (kind, page_size, shuffled)."""
+    parts = text.split(":")
+    if parts[0] == "rows" and len(parts) <= 2 and parts[1:] in ([], ["shuffled"]):
+        return "rows", 1, parts[1:] == ["shuffled"]
+    if parts[0] == "pages" and len(parts) in (2, 3) and parts[1].isdigit() and int(parts[1]) >= 1 \
+            and parts[2:] in ([], ["shuffled"]):
+        return "pages", int(parts[1]), parts[2:] == ["shuffled"]
+    raise SystemExit(f"bad --layout {text!r}: rows, rows:shuffled, pages:N or pages:N:shuffled")
+
+
 def bench_ours(args):
     import mla_decode_attention_09_gb300 as mla
     from mla_decode_attention_09_gb300 import build as mla_build
@@ -230,19 +241,53 @@ def bench_ours(args):
     mla_build.build()
     w = mi.get_workload(args.workload)
     nbytes = mi.workload_bytes(w)
-    step_bytes = nbytes["total"]
+    kind, page_size, shuffled = parse_layout(args.layout)
+    q_len = args.q_len
+    default_layout = kind == "rows" and not shuffled and q_len == 1
+    # algorithmic bytes: KV rows read once, Q read and O written for every query token
+    step_bytes = nbytes["kv"] + (nbytes["q"] + nbytes["o"]) * q_len
 
     # two input copies, each larger than L2 for the headline workload (seeded per rank: independent replicas)
-    devs = [mi.make_workload(w, device=str(dev), seed_offset=replica_seed_offset(rank, k)) for k in range(2)]
+    def make(k):
+        seed = w.seed + replica_seed_offset(rank, k)
+        lens = mi.workload_lengths(w)
+        if kind == "pages":
+            return mi.make_paged_inputs(lens, page_size, w.mode, seed, permute=shuffled, device=str(dev))
+        if shuffled:
+            return mi.make_inputs(lens, w.mode, seed, permute=True, device=str(dev))
+        return mi.make_workload(w, device=str(dev), seed_offset=replica_seed_offset(rank, k))
+
+    devs = [make(k) for k in range(2)]
     scales = [d.kv_scale_tensor(dev) for d in devs]
-    plan = mla.plan(devs[0].kv_indptr.cpu(), 0, num_kv_slots=devs[0].kv.shape[0], fp8_kernel=args.fp8_kernel)
+    opts = {"num_kv_slots": devs[0].kv.shape[0], "fp8_kernel": args.fp8_kernel}
+    last_host = devs[0].kv_last_page_len.cpu() if kind == "pages" else None
+    queries = None
+    if q_len > 1:
+        queries = []
+        for k in range(2):
+            qh, qo = mi.make_query_tokens([q_len] * w.batch, seed=w.seed + 50 + replica_seed_offset(rank, k))
+            queries.append((qh.to(dev), qo.to(dev)))
+        plan = mla.plan_multi(queries[0][1].cpu(), devs[0].kv_indptr.cpu(), causal=True, page_size=page_size,
+                              kv_last_page_len_host=last_host, **opts)
+    elif kind == "pages":
+        plan = mla.plan_paged(devs[0].kv_indptr.cpu(), last_host, page_size, **opts)
+    else:
+        plan = mla.plan(devs[0].kv_indptr.cpu(), 0, **opts)
     info = plan.info()
-    outs = [torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    outs = [torch.empty((w.batch * q_len, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(2)]
 
     def call(k, stream=None):
         d = devs[k]
-        mla.decode(d.q, d.kv, scales[k], d.kv_indptr, d.kv_indices, outs[k], sm_scale=d.sm_scale,
-                   dtype_mode=w.mode, plan=plan, stream=stream, validate=False)
+        if queries is not None:
+            mla.decode_multi(queries[k][0], d.kv, scales[k], queries[k][1], d.kv_indptr, d.kv_indices, outs[k],
+                             plan=plan, kv_last_page_len=d.kv_last_page_len if kind == "pages" else None,
+                             sm_scale=d.sm_scale, dtype_mode=w.mode, stream=stream, validate=False)
+        elif kind == "pages":
+            mla.decode_paged(d.q, d.kv, scales[k], d.kv_indptr, d.kv_indices, d.kv_last_page_len, page_size, outs[k],
+                             sm_scale=d.sm_scale, dtype_mode=w.mode, plan=plan, stream=stream, validate=False)
+        else:
+            mla.decode(d.q, d.kv, scales[k], d.kv_indptr, d.kv_indices, outs[k], sm_scale=d.sm_scale,
+                       dtype_mode=w.mode, plan=plan, stream=stream, validate=False)
 
     for k in range(max(args.warmup, 3)):
         call(k % 2)
@@ -299,17 +344,23 @@ def bench_ours(args):
     launches_per_step = 1 + (1 if info["num_split_seqs"] > 0 else 0)
 
     # roofline of the dominant kernel: stage 1 alone, each launch bracketed by events on its stream
+    # (the row layout has a stage-1-only entry point; other layouts bracket the whole call)
     n_roof = max(8, min(args.steps, 200))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_roof)]
     torch.cuda.synchronize()
     torch.cuda._sleep(200_000_000)  # keep the GPU busy while the launches below are queued: no host gaps
+    stage1_only = kind == "rows" and q_len == 1
     for i in range(n_roof):
         d = devs[i % 2]
         ev[i][0].record()
-        mla.decode_stage1(d.q, d.kv, scales[i % 2], d.kv_indptr, d.kv_indices, outs[i % 2], plan=plan,
-                          sm_scale=d.sm_scale, dtype_mode=w.mode)
+        if stage1_only:
+            mla.decode_stage1(d.q, d.kv, scales[i % 2], d.kv_indptr, d.kv_indices, outs[i % 2], plan=plan,
+                              sm_scale=d.sm_scale, dtype_mode=w.mode)
+        else:
+            call(i % 2)
         ev[i][1].record()
-        mla.decode_reduce(outs[i % 2], plan=plan)
+        if stage1_only:
+            mla.decode_reduce(outs[i % 2], plan=plan)
     torch.cuda.synchronize()
     stage1_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     peak, peak_kind = measured_peak()
@@ -317,15 +368,19 @@ def bench_ours(args):
     kernel = ("mla_stage1_fp8_umma_kernel" if (w.mode == mi.MODE_FP8 and args.fp8_kernel == 0)
               else "mla_stage1_kernel")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kernel, args.workload),
+                "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(kernel, args.workload) if default_layout else None,
                 "kernel": kernel, "peak_kind": peak_kind,
-                "algorithmic_bytes_per_launch": step_bytes, "stage1_us": round(stage1_ms * 1e3, 2)}
+                "algorithmic_bytes_per_launch": step_bytes,
+                "stage1_us" if stage1_only else "call_us": round(stage1_ms * 1e3, 2)}
 
+    # end to end and the oracle baseline are measured on the row layout with one query token
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and default_layout:
         e2e = bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes)
     assert plan.check_error() == 0
-    host0 = devs[0].to("cpu") if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    host0 = (devs[0].to("cpu") if (rank == 0 and ws == 1 and not args.no_cpu_baseline and default_layout)
+             else None)
 
     cpu = None
     if host0 is not None:
@@ -341,7 +396,9 @@ def bench_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {mi.MODE_BF16: "bf16", mi.MODE_FP8: "e4m3", mi.MODE_A16W8: "f16"}[w.mode], "data": "synthetic",
         "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
-                   "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": 1, "bytes_per_call": step_bytes,
+                   "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": page_size,
+                   "kv_order": "shuffled" if shuffled else ("workload" if kind == "rows" else "in order"),
+                   "q_len": q_len, "causal": q_len > 1, "bytes_per_call": step_bytes,
                    "l2": "inputs larger than L2, two copies alternate", "timing": "CUDA graphs of decode calls",
                    "plan": {k: info[k] for k in ("num_ctas", "num_work_items", "num_split_seqs")},
                    "fp8_kernel": ("tcgen05" if args.fp8_kernel == 0 else "mma.sync") if w.mode == mi.MODE_FP8 else None},
@@ -349,7 +406,7 @@ def bench_ours(args):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
-    if args.all_workloads and rank == 0:
+    if args.all_workloads and rank == 0 and default_layout:
         line["per_workload"] = per_workload(mla, dev, fp8_kernel=args.fp8_kernel)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -404,7 +461,7 @@ def per_workload(mla, dev, calls: int = 200, fp8_kernel: int = 0):
     scrub write would leave dirty lines that the timed call must write back)."""
     res = {}
     scrub = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty(1, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     for name, w in mi.WORKLOADS.items():
         inp = mi.make_workload(w, device=str(dev))
         ks = inp.kv_scale_tensor(dev)
@@ -491,6 +548,9 @@ def main():
     ap.add_argument("--fp8-kernel", type=int, default=0, choices=[0, 1],
                     help="fp8 stage-1 kernel: 0 tcgen05/TMA (default), 1 warp-level mma.sync")
     ap.add_argument("--cpu-sample-seqs", type=int, default=8)
+    ap.add_argument("--layout", default="rows",
+                    help="KV layout of the workload: rows (its own order), rows:shuffled, pages:N, pages:N:shuffled")
+    ap.add_argument("--q-len", type=int, default=1, help="query tokens per sequence (causal)")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

@@ -101,3 +101,14 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert np.isfinite(d["ms_per_step"])
+
+
+def test_bench_layout_option():
+    import bench
+    assert bench.parse_layout("rows") == ("rows", 1, False)
+    assert bench.parse_layout("rows:shuffled") == ("rows", 1, True)
+    assert bench.parse_layout("pages:64") == ("pages", 64, False)
+    assert bench.parse_layout("pages:8:shuffled") == ("pages", 8, True)
+    for bad in ("pages", "pages:0", "pages:x", "rows:3", "pages:8:sorted", "grid"):
+        with pytest.raises(SystemExit):
+            bench.parse_layout(bad)
