@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             const uint8_t* kv8 = static_cast<const uint8_t*>(a.kv);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-#pragma unroll 2
+#pragma unroll 4
               for (int rr = (g + kLoaders - (32 * j) % kLoaders) % kLoaders; rr < 32; rr += kLoaders) {
                 const int r = 32 * j + rr;
                 const int yr = __shfl_sync(~0u, y0s[j], rr);
