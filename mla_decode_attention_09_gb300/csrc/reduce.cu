@@ -6,10 +6,11 @@
 // out = sum_s 2^{lse_s - L} O_s, rounded to bf16.
 //
 // One CTA of 128 threads per (split sequence, head); each thread owns 4 of the
-// 512 output dims, so every partial row is read once with 16-byte loads. Every
-// warp finds the max and the sum of 2^(lse - max) with one slot per lane, and
-// the partial rows are read eight slots at a time so that several loads are in
-// flight per thread.
+// 512 output dims, so every partial row is read once with 16-byte loads. Rows
+// of up to eight slots (the usual case) take one round trip: every thread loads
+// all their LSEs and its parts of all their partial rows at once. Longer rows
+// find the max and the sum of 2^(lse - max) with one slot per lane, and read
+// the partial rows eight slots at a time.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,18 +44,47 @@ __global__ void __launch_bounds__(kReduceThreads)
   const int n = r.n_slots;
   const float* lse = p.part_lse + (int64_t)r.slot_begin * kHeads + h;
   float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[(int64_t)s * kHeads]);
+  if (n > kUnroll) {
+    for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[(int64_t)s * kHeads]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (m != -INFINITY) {
+  constexpr int64_t kSlotStride = (int64_t)kHeads * kVDim;
+  const float* po = p.part_o + ((int64_t)r.slot_begin * kHeads + h) * kVDim + 4 * threadIdx.x;
+  if (n <= kUnroll) {
+    float4 v[kUnroll];
+    float ls[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (u < n) {
+        ls[u] = lse[(int64_t)u * kHeads];
+        v[u] = __ldcs(reinterpret_cast<const float4*>(po + u * kSlotStride));
+      } else {
+        ls[u] = -INFINITY;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) mx = fmaxf(mx, ls[u]);
+    if (mx != -INFINITY) {
+      float wt[kUnroll], z = 0.f;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        wt[u] = exp2f(ls[u] - mx);  // 0 for the unused slots
+        z += wt[u];
+      }
+      const float inv_z = 1.0f / z;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) fma4(acc, wt[u] * inv_z, v[u]);
+    }
+  } else if (m != -INFINITY) {
     float z = 0.f;
     for (int s = lane; s < n; s += 32) z += exp2f(lse[(int64_t)s * kHeads] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(~0u, z, o);
     const float inv_z = 1.0f / z;
-    const float* po = p.part_o + ((int64_t)r.slot_begin * kHeads + h) * kVDim + 4 * threadIdx.x;
-    constexpr int64_t kSlotStride = (int64_t)kHeads * kVDim;
     for (int s0 = 0; s0 < n; s0 += 32) {
       // lane j holds the weight of slot s0 + j
       const int cnt = min(32, n - s0);
