@@ -99,6 +99,11 @@ typedef struct mla_plan_options {
                              loader warps (default); 1 = one issuing thread and three loader warps, a
                              few per cent faster only when the KV rows of page-size-1 sequences are
                              scattered one by one. 0 = default. Results are identical either way. */
+  int item_cost_rows;     /* balancing: each work item a CTA starts (a sequence piece, per query token)
+                             counts as this many extra KV rows when the planner evens out the CTAs'
+                             work (an item boundary costs an epilogue and a pipeline refill). 0 = default
+                             (256, about two tiles' time measured on fp8 B=64 L=8192); negative = none,
+                             which divides the rows alone evenly. */
 } mla_plan_options;
 
 /* Read-only description of a plan. */

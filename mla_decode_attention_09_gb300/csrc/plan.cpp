@@ -33,6 +33,8 @@ PlanOptions resolve_options(const mla_plan_options* o) {
   if (o->ctas_per_sm > 0) r.ctas_per_sm = o->ctas_per_sm;
   if (o->fp8_kernel == 1) r.fp8_kernel = 1;
   if (o->fp8_issuers == 1 || o->fp8_issuers == 2) r.fp8_issuers = o->fp8_issuers;
+  if (o->item_cost_rows > 0) r.item_cost_rows = o->item_cost_rows;
+  if (o->item_cost_rows < 0) r.item_cost_rows = 0;
   return r;
 }
 
@@ -66,37 +68,77 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
 
   // Work is counted in granules: sequence b is ceil(L_b / G) granules of G
   // rows (its last one may be shorter), each weighing the number of query
-  // tokens that read it. The weighted granules of all sequences, laid end to
-  // end, are divided evenly among the ranges, so every range gets the same
-  // weight to within one query token's granule and every cut falls on a
-  // multiple of G rows from its sequence's start. With one query token per
-  // sequence and G equal to the kernels' tile height, the ranges hold the same
-  // number of tiles to within one. A range reads each of its KV rows from HBM
-  // once: the query tokens of one sequence are processed back to back on the
-  // same rows, which the later ones find in L2.
+  // tokens that read it. Every item a range starts (one per query token of each
+  // sequence piece it holds) adds a fixed cost of item_cost_rows rows: an item
+  // boundary costs a CTA an epilogue, a query staging and a pipeline refill,
+  // measured at about two tiles' time. Ranges are cut, on multiples of G rows
+  // from each sequence's start, so that the largest range cost is as small as
+  // the number of CTAs allows (binary search on that cost, filling greedily).
+  // With one query token per sequence, no item cost and G equal to the
+  // kernels' tile height, the ranges hold the same number of tiles to within
+  // one. A range reads each of its KV rows from HBM once; the query tokens of
+  // one sequence run back to back over the same rows.
   const int64_t G = opt.granularity;
   const int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
-  std::vector<int64_t> gstart((size_t)batch + 1, 0);
-  for (int b = 0; b < batch; ++b)
-    gstart[(size_t)b + 1] = gstart[(size_t)b] + (seq_len(b) + G - 1) / G * n_queries(b);
-  const int64_t U = gstart[(size_t)batch];
-  int64_t target = U > 0 ? (U + max_ctas - 1) / max_ctas : 1;
-  target = std::max<int64_t>(target, (opt.min_rows_per_split + G - 1) / G);
-  const int64_t n_ranges = U > 0 ? std::min<int64_t>(max_ctas, (U + target - 1) / target) : 1;
-
-  std::vector<int64_t> cuts((size_t)n_ranges + 1, 0);
-  cuts[(size_t)n_ranges] = total;
-  for (int64_t k = 1; k < n_ranges; ++k) {
-    const int64_t g = U * k / n_ranges;
-    // sequence holding weighted granule g: last b with gstart[b] <= g (it has weight since g < U)
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) / 2;
-      if (gstart[(size_t)mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    const int64_t S = tok[(size_t)lo], L = seq_len(lo);
-    cuts[(size_t)k] = S + std::min<int64_t>((g - gstart[(size_t)lo]) / n_queries(lo) * G, L);
+  const int64_t kUnit = 16;  // cost units per granule, so that an item cost below one granule still counts
+  const int64_t item_cost = (int64_t)opt.item_cost_rows * kUnit / G;
+  const int64_t min_granules = (opt.min_rows_per_split + G - 1) / G;
+  std::vector<int64_t> ngran((size_t)batch, 0);
+  int64_t U = 0, n_pieces_min = 0;
+  for (int b = 0; b < batch; ++b) {
+    ngran[(size_t)b] = (seq_len(b) + G - 1) / G;
+    U += ngran[(size_t)b] * n_queries(b);
+    if (ngran[(size_t)b] > 0 && n_queries(b) > 0) n_pieces_min += n_queries(b);
   }
+  // Greedy fill for a largest range cost T: the number of ranges it needs and,
+  // when starts is given, the row where each range after the first begins. A
+  // piece of a split sequence is min_granules long at least: a range that
+  // could take less closes first, and a remainder shorter than that stays in
+  // the range that holds the rest (which may then exceed T).
+  auto fill = [&](int64_t T, std::vector<int64_t>* starts) {
+    int64_t n = 1, cur = 0;
+    bool empty = true;
+    auto close = [&](int b, int64_t rem) {
+      ++n;
+      cur = 0;
+      empty = true;
+      if (starts) starts->push_back(tok[(size_t)b] + (ngran[(size_t)b] - rem) * G);
+    };
+    for (int b = 0; b < batch; ++b) {
+      const int64_t w = n_queries(b) * kUnit, a = n_queries(b) * item_cost;
+      int64_t rem = ngran[(size_t)b];
+      if (rem == 0 || w == 0) continue;
+      while (rem > 0) {
+        int64_t fit = T > cur + a ? (T - cur - a) / w : 0;
+        if (!empty && fit < std::min(rem, min_granules)) {
+          close(b, rem);
+          fit = T > a ? (T - a) / w : 0;
+        }
+        int64_t take = std::max<int64_t>(std::min(rem, fit), std::min(rem, min_granules));
+        if (rem - take > 0 && rem - take < min_granules) take = rem;
+        cur += a + take * w;
+        empty = false;
+        rem -= take;
+        if (rem > 0) close(b, rem);
+      }
+    }
+    return n;
+  };
+  std::vector<int64_t> cuts{0};
+  if (U > 0) {
+    // smallest T whose greedy fill needs at most max_ctas ranges, and ranges of min_granules at least
+    int64_t lo = std::max<int64_t>((U * kUnit + max_ctas - 1) / max_ctas, 1);
+    lo = std::max<int64_t>(lo, min_granules * kUnit);
+    int64_t hi = std::max<int64_t>(U * kUnit + n_pieces_min * item_cost * 2 + item_cost, lo);
+    while (fill(hi, nullptr) > max_ctas) hi *= 2;
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (fill(mid, nullptr) <= max_ctas) hi = mid; else lo = mid + 1;
+    }
+    fill(lo, &cuts);
+  }
+  cuts.push_back(total);
+  const int64_t n_ranges = (int64_t)cuts.size() - 1;
   std::vector<std::pair<int64_t, int64_t>> ranges;  // non-empty CTA row ranges, in order
   for (int64_t k = 0; k < n_ranges; ++k)
     if (cuts[(size_t)k + 1] > cuts[(size_t)k]) ranges.emplace_back(cuts[(size_t)k], cuts[(size_t)k + 1]);

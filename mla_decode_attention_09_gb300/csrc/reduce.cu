@@ -34,13 +34,14 @@ __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
 
 __global__ void __launch_bounds__(kReduceThreads)
     mla_reduce_kernel(const DevicePlan p, __nv_bfloat16* __restrict__ out, int use_pdl) {
+  const int e = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
+  // the plan's reduce map was written when the plan was made: read it while stage 1 finishes
+  const ReduceEntry r = e < p.n_reduce ? p.reduce[e] : ReduceEntry{0, 0, 0, 0};
   if (use_pdl) ptx::griddep_wait();  // stage 1 of this decode has finished writing the partials
   // the next kernel in the stream may start its prologue; it waits for this grid before touching memory
   ptx::griddep_launch_dependents();
-  const int e = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
   if (e >= p.n_reduce) return;
   const int lane = threadIdx.x & 31;
-  const ReduceEntry r = p.reduce[e];
   const int n = r.n_slots;
   const float* lse = p.part_lse + (int64_t)r.slot_begin * kHeads + h;
   float m = -INFINITY;

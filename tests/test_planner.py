@@ -5,6 +5,21 @@ import pytest
 import mla_decode_attention_09_gb300 as mla
 
 
+def _even_split_costs(gl, n_ctas, item_units, unit):
+    """Costs of the ranges that cut the granules of all sequences, laid end to end, evenly:
+    range k holds granules [U k / n, U (k + 1) / n); a sequence it touches adds one item."""
+    U = sum(gl)
+    starts = np.cumsum([0] + gl)
+    costs = []
+    for k in range(n_ctas):
+        a, b = U * k // n_ctas, U * (k + 1) // n_ctas
+        if b <= a:
+            continue
+        touched = sum(1 for i, g in enumerate(gl) if g and starts[i] < b and starts[i] + g > a)
+        costs.append((b - a) * unit + touched * item_units)
+    return costs
+
+
 def _check_plan(lengths, num_sms, **opts):
     ip = np.zeros(len(lengths) + 1, dtype=np.int32)
     ip[1:] = np.cumsum(lengths)
@@ -43,19 +58,38 @@ def _check_plan(lengths, num_sms, **opts):
             next_slot += n
             assert all(t1 > t0 for t0, t1, _ in parts), "no empty partial"
     assert next_slot == r["num_slots"]
-    # load balance in granules (G rows; a sequence's last granule may be shorter): every CTA
-    # holds floor or ceil of (granules / CTAs), and no CTA more than the target
+    # Load balance. A CTA's cost is its granules (G rows; a sequence's last granule may be
+    # shorter) plus a fixed cost per item it starts (item_cost_rows, default 256 rows). The
+    # planner minimises the largest cost: it is never above that of cutting the granules
+    # evenly, which is checked when the minimum split is one granule. Without item costs
+    # that means at most ceil(granules / CTAs) granules per CTA.
     if total:
         max_ctas = num_sms * cpsm
-        U = sum(-(-L // G) for L in lengths)
-        target = max(-(-U // max_ctas), -(-min_split // G))
+        ic = opts.get("item_cost_rows", 0)
+        ic = 256 if ic == 0 else max(ic, 0)
+        unit = 16
+        item_units = ic * unit // G
+        min_gran = -(-min_split // G)
+        gl = [-(-L // G) for L in lengths]
+        U = sum(gl)
         gran = [sum(-(-int(items[i, 2] - items[i, 1]) // G) for i in range(wip[c], wip[c + 1]))
                 for c in range(r["num_ctas"])]
+        nit = [sum(1 for i in range(wip[c], wip[c + 1]) if items[i, 2] > items[i, 1]) for c in range(r["num_ctas"])]
+        cost = [g * unit + n * item_units for g, n in zip(gran, nit)]
         assert sum(gran) == U
-        assert max(gran) <= target
-        assert max(gran) - min(gran) <= 1
         rows = [sum(int(items[i, 2] - items[i, 1]) for i in range(wip[c], wip[c + 1])) for c in range(r["num_ctas"])]
         assert sum(rows) == total
+        if min_gran == 1:
+            assert max(cost) <= max(_even_split_costs(gl, max_ctas, item_units, unit))
+            if ic == 0:
+                assert max(gran) <= -(-U // max_ctas)
+        else:
+            # every piece of a split sequence holds min_rows_per_split rows at least, unless it
+            # is the sequence's last piece and the whole remainder
+            for b in range(len(lengths)):
+                parts = [(int(t0), int(t1)) for bb, t0, t1, _, _ in items if bb == b]
+                if len(parts) > 1:
+                    assert all(t1 - t0 >= min(min_gran * G, lengths[b]) for t0, t1 in parts[:-1])
     return r
 
 
@@ -84,18 +118,29 @@ def test_plan_invariants_random():
 
 
 def test_plan_headline_shapes():
-    # B=64 x 8192 over 152 SMs: every SM busy, each sequence split in 2-4 chunks
+    # B=64 x 8192 over 152 SMs: (nearly) every SM busy, each sequence split in 2-4 chunks
     r = _check_plan([8192] * 64, 152)
-    assert r["num_ctas"] == 152
+    assert 150 <= r["num_ctas"] <= 152
     assert 64 * 2 <= r["num_slots"] <= 64 * 4
     # B=4 x 1024 bf16: small problem, one 128-row tile per CTA (the minimum chunk)
     r = _check_plan([1024] * 4, 152)
     assert r["num_ctas"] == 32
-    # every CTA gets 26 or 27 of the 4096 tiles of B=64 x 8192
-    r = mla.plan_compute_host(np.arange(65, dtype=np.int32) * 8192, 152)
-    tiles = [sum(-(-int(t1 - t0) // 128) for _, t0, t1, _, _ in r["items"][r["work_indptr"][c]:r["work_indptr"][c + 1]])
-             for c in range(152)]
-    assert set(tiles) <= {26, 27}
+    # B=64 x 8192, 4096 tiles. Without item costs every CTA gets 27 tiles at most. With the
+    # default cost of two tiles per item, CTAs that hold two sequence pieces get fewer tiles
+    # than those holding one, and the largest cost (tiles + 2 x items) drops from 31 to 30.
+    def tiles_items(r):
+        t, n = [], []
+        for c in range(r["num_ctas"]):
+            its = r["items"][r["work_indptr"][c]:r["work_indptr"][c + 1]]
+            t.append(sum(-(-int(t1 - t0) // 128) for _, t0, t1, _, _ in its))
+            n.append(len(its))
+        return np.array(t), np.array(n)
+    ip = np.arange(65, dtype=np.int32) * 8192
+    t, n = tiles_items(mla.plan_compute_host(ip, 152, item_cost_rows=-1))
+    assert t.sum() == 4096 and t.max() == 27 and (t + 2 * n).max() == 31
+    t, n = tiles_items(mla.plan_compute_host(ip, 152))
+    assert t.sum() == 4096 and (t + 2 * n).max() == 30 and len(t) >= 150
+    assert t[n == 2].max() < t[n == 1].max()
 
 
 def test_plan_rejects_bad_indptr():
@@ -220,12 +265,13 @@ def test_multi_plan_balances_weighted_granules():
     ip[1:] = np.cumsum(lengths)
     qo = np.zeros(len(q_lens) + 1, dtype=np.int32)
     qo[1:] = np.cumsum(q_lens)
-    r = mla.plan_compute_host_multi(qo, ip, 20, causal=False)
+    r = mla.plan_compute_host_multi(qo, ip, 20, causal=False, item_cost_rows=-1)
     items, wip = r["items"], r["work_indptr"]
     w = [sum(-(-int(items[i, 2] - items[i, 1]) // 128) for i in range(wip[c], wip[c + 1]))
          for c in range(r["num_ctas"])]
-    assert sum(w) == sum(-(-L // 128) * q for L, q in zip(lengths, q_lens))
-    assert max(w) - min(w) <= 4  # one granule of the heaviest sequence
+    U = sum(-(-L // 128) * q for L, q in zip(lengths, q_lens))
+    assert sum(w) == U
+    assert max(w) <= -(-U // 20) + 3  # the even share, plus less than one granule of the heaviest sequence
 
 
 def test_multi_plan_rejects_bad_query_offsets():
