@@ -324,8 +324,9 @@ int mla_plan_compute_host_paged(int batch, const int32_t* kv_indptr_host, const 
  * addressing.
  *
  * The work is planned per sequence: one CTA processes every query token of a
- * sequence on the same KV rows back to back, so a row is read from HBM once
- * and from L2 for the other tokens.
+ * sequence on the same KV rows back to back. The later tokens find the rows in
+ * L2 only when the CTAs' ranges fit in it; at B=64, kv_len=8192 they do not, and
+ * each token's pass reads the rows from HBM.
  *
  * mla_decode_plan_multi — the planner for that layout (host arrays as for
  *   mla_decode_plan_paged, plus qo_indptr_host [B+1], 0 first, non-decreasing).
