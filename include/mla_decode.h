@@ -96,9 +96,9 @@ typedef struct mla_plan_options {
   int fp8_kernel;         /* fp8 stage-1 kernel: 0 = 5th-generation tensor cores (tcgen05 + TMA, default),
                              1 = warp-level mma.sync (kept for comparison) */
   int fp8_issuers;        /* tcgen05 kernel's MMA issue: 2 = two issuing threads (scores, P.V) and two
-                             loader warps (default); 1 = one issuing thread and three loader warps, a
-                             few per cent faster only when the KV rows of page-size-1 sequences are
-                             scattered one by one. 0 = default. Results are identical either way. */
+                             loader warps (default, faster on every layout measured); 1 = one issuing
+                             thread and three loader warps, kept for comparison. 0 = default. Results
+                             are identical either way. */
   int item_cost_rows;     /* balancing: each work item a CTA starts (a sequence piece, per query token)
                              counts as this many extra KV rows when the planner evens out the CTAs'
                              work (an item boundary costs an epilogue and a pipeline refill). 0 = default
