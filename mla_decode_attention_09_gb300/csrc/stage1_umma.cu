@@ -29,9 +29,9 @@
 // Two in-order chains go faster than one: a single thread issues a small-N
 // tcgen05.mma about every 46-58 cycles, the tensor core takes one every ~39.
 // With one issuer, lane 0 of warp 5 polls both chains and warps 6 and 7 are
-// loaders, which keeps HBM busier when every tile is copied row by row (one
-// warp cannot issue those copies fast enough; three come close). The latent
-// part of a tile
+// loaders; it measured slower on every layout and is kept for comparison.
+// The first item's query is staged by warps 0-3, later ones by warp 4. The
+// latent part of a tile
 // (512 B per row, needed until P.V finishes) lives in a 3-slot ring of 64 KB,
 // the rope part (64 B per row, needed only by the scores) in a 2-slot ring of
 // 8 KB, so three tiles can be resident or in flight. S, P and O are double
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // ------------------------------------------------ loaders: KV tiles (+ query staging in warp 4)
     // Every loader walks the same tile stream and takes the same box / row-copy
     // decision from the same indices. Warp 4 issues the box loads; the row copies
-    // of a scattered tile are split among the three loaders. Every loader waits
+    // of a scattered tile are split among the loaders. Every loader waits
     // for every tile's slot and arrives on every tile's full barrier: the loaders
     // then stay in lockstep with the slot barriers, whose parity waits cannot
     // tell a phase from the one two later.
@@ -527,8 +527,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
               if (lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
             }
           } else {
-            // Row r's index sits in lane (r & 31), slot (r >> 5); loader g copies the
-            // latent rows r = g mod 3 and the rope groups i = g mod 3. Latent: lane l
+            // Row r's index sits in lane (r & 31), slot (r >> 5); loader g of n copies the
+            // latent rows r = g mod n and the rope groups i = g mod n. Latent: lane l
             // copies 16-byte chunk l of the row's 512 bytes into column block l / 8 at
             // chunk (l % 8) ^ (r % 8) (the 128-byte swizzle). Rope: 8 rows per
             // instruction, lane l copies chunk l % 4 of row 8i + l / 4 at chunk
