@@ -90,6 +90,30 @@ def test_one_long_sequence_many_splits(mla, mode, k8):
 
 
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+def test_many_short_sequences(mla, mode, k8):
+    # 3000 sequences of 0..200 rows at random slots: many items per CTA, with empty and
+    # one-row sequences among them; 80 sequences are compared (first, last, and a sample)
+    rng = np.random.default_rng(77 + mode)
+    lengths = [int(x) for x in rng.integers(0, 201, 3000)]
+    lengths[5] = 0
+    lengths[6] = 1
+    inp = mi.make_inputs(lengths, mode, seed=400 + mode, permute=True)
+    out, plan = run(mla, inp, **k8)
+    assert plan.check_error() == 0
+    ids = sorted({0, 5, 6, 2999} | {int(x) for x in rng.choice(3000, 76, replace=False)})
+    compare(out[torch.tensor(ids, device="cuda")], oracle_out(inp, seq_ids=ids), mode, "many short sequences")
+
+
+@pytest.mark.parametrize("mode,k8", [(mi.MODE_BF16, {}), (mi.MODE_FP8, {})], ids=["bf16", "fp8-tcgen05"])
+def test_one_very_long_sequence(mla, mode, k8):
+    # 300,000 rows in one sequence, split over every CTA by the default plan
+    inp = mi.make_inputs([300_000], mode, seed=500 + mode)
+    out, plan = run(mla, inp, **k8)
+    assert plan.info()["num_ctas"] >= 100
+    compare(out, oracle_out(inp), mode, "one very long sequence")
+
+
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_peaked_scores(mla, mode, k8):
     # larger query norm -> sharply peaked softmax; exercises the running-max rescale
     inp = mi.make_inputs([300, 1, 77, 2000], mode, seed=9, q_std=6.0)
