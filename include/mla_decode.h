@@ -104,6 +104,11 @@ typedef struct mla_plan_options {
                              work (an item boundary costs an epilogue and a pipeline refill). 0 = default
                              (256, about two tiles' time measured on fp8 B=64 L=8192); negative = none,
                              which divides the rows alone evenly. */
+  int token_parallel;     /* several query tokens (mla_decode_plan_multi): when every sequence with KV rows
+                             has the same number Q > 1 of query tokens, plan the row ranges for one
+                             token and give each range Q CTAs, one per token, which read the same rows
+                             at the same time (from HBM once, from L2 for the others). 0 = default (on);
+                             negative = off: each range's tokens run back to back in one CTA. */
 } mla_plan_options;
 
 /* Read-only description of a plan. */

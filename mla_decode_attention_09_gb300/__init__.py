@@ -55,7 +55,8 @@ class MLAError(RuntimeError):
 class PlanOptions(ctypes.Structure):
     _fields_ = [("num_kv_slots", ctypes.c_int64), ("min_rows_per_split", ctypes.c_int),
                 ("granularity", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("fp8_kernel", ctypes.c_int),
-                ("fp8_issuers", ctypes.c_int), ("item_cost_rows", ctypes.c_int)]
+                ("fp8_issuers", ctypes.c_int), ("item_cost_rows", ctypes.c_int),
+                ("token_parallel", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -126,9 +127,9 @@ def _check(status: int, what: str):
 
 
 def _opts(num_kv_slots=0, min_rows_per_split=0, granularity=0, ctas_per_sm=0, fp8_kernel=0,
-          fp8_issuers=0, item_cost_rows=0) -> PlanOptions:
+          fp8_issuers=0, item_cost_rows=0, token_parallel=0) -> PlanOptions:
     return PlanOptions(int(num_kv_slots), int(min_rows_per_split), int(granularity), int(ctas_per_sm),
-                       int(fp8_kernel), int(fp8_issuers), int(item_cost_rows))
+                       int(fp8_kernel), int(fp8_issuers), int(item_cost_rows), int(token_parallel))
 
 
 def _host_indptr(kv_indptr) -> torch.Tensor:

@@ -63,6 +63,7 @@ bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, c
          p->opt.min_rows_per_split == o.min_rows_per_split && p->opt.granularity == o.granularity &&
          p->opt.ctas_per_sm == o.ctas_per_sm && p->opt.fp8_kernel == o.fp8_kernel &&
          p->opt.fp8_issuers == o.fp8_issuers && p->opt.item_cost_rows == o.item_cost_rows &&
+         p->opt.token_parallel == o.token_parallel &&
          std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0 &&
          same_array(p->last_page_len, l.last, (size_t)batch) &&
          same_array(p->qo_indptr, l.qo, batch > 0 ? (size_t)batch + 1 : 0);

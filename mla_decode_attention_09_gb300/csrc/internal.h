@@ -65,6 +65,7 @@ struct PlanOptions {
   int fp8_kernel = 0;  // 0 = tcgen05 / TMA kernel, 1 = warp-level mma.sync kernel
   int fp8_issuers = 0;  // tcgen05 kernel: 0 or 2 two MMA-issuing threads, 1 one issuer + three loaders
   int item_cost_rows = 256;  // balancing cost of each item a CTA starts, in KV rows (0 = none)
+  bool token_parallel = true;  // multi-token plans with equal query counts: one CTA per (range, token)
 };
 
 // Two MMA-issuing threads in the tcgen05 kernel unless asked for one: one

@@ -35,6 +35,7 @@ PlanOptions resolve_options(const mla_plan_options* o) {
   if (o->fp8_issuers == 1 || o->fp8_issuers == 2) r.fp8_issuers = o->fp8_issuers;
   if (o->item_cost_rows > 0) r.item_cost_rows = o->item_cost_rows;
   if (o->item_cost_rows < 0) r.item_cost_rows = 0;
+  if (o->token_parallel < 0) r.token_parallel = false;
   return r;
 }
 
@@ -79,16 +80,32 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   // one. A range reads each of its KV rows from HBM once; the query tokens of
   // one sequence run back to back over the same rows.
   const int64_t G = opt.granularity;
-  const int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
+  int64_t max_ctas = (int64_t)num_sms * opt.ctas_per_sm;
   const int64_t kUnit = 16;  // cost units per granule, so that an item cost below one granule still counts
   const int64_t item_cost = (int64_t)opt.item_cost_rows * kUnit / G;
   const int64_t min_granules = (opt.min_rows_per_split + G - 1) / G;
   std::vector<int64_t> ngran((size_t)batch, 0);
+  for (int b = 0; b < batch; ++b) ngran[(size_t)b] = (seq_len(b) + G - 1) / G;
+  // Token-parallel plans: when every sequence with KV rows has the same number Q > 1
+  // of query tokens, the row ranges are planned for one token over max_ctas / Q
+  // CTAs, and each range becomes Q CTAs, one per query token, side by side in the
+  // grid. They read the same rows at the same time: the rows come from HBM once
+  // and from L2 for the other tokens (a range processing its tokens back to back
+  // re-reads them from HBM once the ranges outgrow L2).
+  int64_t Qu = 0;
+  bool uniform = true;
+  for (int b = 0; b < batch; ++b) {
+    if (ngran[(size_t)b] == 0 || n_queries(b) == 0) continue;
+    if (Qu == 0) Qu = n_queries(b);
+    else if (n_queries(b) != Qu) uniform = false;
+  }
+  const bool token_par = opt.token_parallel && uniform && Qu > 1 && max_ctas / Qu >= 1;
+  if (token_par) max_ctas /= Qu;
+  auto weight = [&](int b) { return token_par ? (int64_t)1 : n_queries(b); };  // query tokens per range
   int64_t U = 0, n_pieces_min = 0;
   for (int b = 0; b < batch; ++b) {
-    ngran[(size_t)b] = (seq_len(b) + G - 1) / G;
-    U += ngran[(size_t)b] * n_queries(b);
-    if (ngran[(size_t)b] > 0 && n_queries(b) > 0) n_pieces_min += n_queries(b);
+    U += ngran[(size_t)b] * weight(b);
+    if (ngran[(size_t)b] > 0 && n_queries(b) > 0) n_pieces_min += weight(b);
   }
   // Greedy fill for a largest range cost T: the number of ranges it needs and,
   // when starts is given, the row where each range after the first begins. A
@@ -105,7 +122,7 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
       if (starts) starts->push_back(tok[(size_t)b] + (ngran[(size_t)b] - rem) * G);
     };
     for (int b = 0; b < batch; ++b) {
-      const int64_t w = n_queries(b) * kUnit, a = n_queries(b) * item_cost;
+      const int64_t w = weight(b) * kUnit, a = weight(b) * item_cost;
       int64_t rem = ngran[(size_t)b];
       if (rem == 0 || w == 0) continue;
       while (rem > 0) {
@@ -147,12 +164,12 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   std::vector<WorkItem> items;
   std::vector<int32_t> cta_of_item;
   items.reserve((size_t)qo[(size_t)batch] + ranges.size() * 2);
-  size_t cta = 0;
+  size_t cta = 0;  // range index
   const size_t last = ranges.size() - 1;
   auto push = [&](int b, int64_t t0, int64_t t1, int64_t j) {
     items.push_back(WorkItem{b, (int32_t)t0, (int32_t)t1, -1, (int32_t)seq_len(b), (int32_t)(qo[(size_t)b] + j),
                              (int32_t)j, 0});
-    cta_of_item.push_back((int32_t)cta);
+    cta_of_item.push_back((int32_t)(token_par ? (int64_t)cta * Qu + j : (int64_t)cta));
   };
   for (int b = 0; b < batch; ++b) {
     const int64_t S = tok[(size_t)b], E = tok[(size_t)b + 1], q_b = n_queries(b);
@@ -171,7 +188,20 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
       ++cta;
     }
   }
-  const int64_t used_ctas = (int64_t)ranges.size();
+  const int64_t used_ctas = (int64_t)ranges.size() * (token_par ? Qu : 1);
+  if (token_par) {  // group the items by CTA, keeping each CTA's items (and each row's pieces) in order
+    std::vector<size_t> order(items.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) { return cta_of_item[x] < cta_of_item[y]; });
+    std::vector<WorkItem> sorted_items(items.size());
+    std::vector<int32_t> sorted_cta(items.size());
+    for (size_t i = 0; i < order.size(); ++i) {
+      sorted_items[i] = items[order[i]];
+      sorted_cta[i] = cta_of_item[order[i]];
+    }
+    items.swap(sorted_items);
+    cta_of_item.swap(sorted_cta);
+  }
 
   // Partial slots for query rows cut into several items, consecutive per row, rows in order.
   const size_t n_rows = (size_t)qo[(size_t)batch];

@@ -280,3 +280,37 @@ def test_multi_plan_rejects_bad_query_offsets():
         with pytest.raises(mla.MLAError) as e:
             mla.plan_compute_host_multi(np.array(bad, dtype=np.int32), ip, 4)
         assert e.value.status == -10
+
+
+def test_multi_plan_token_parallel():
+    """Equal query counts: the row ranges are planned for one token, and CTAs r*Q .. r*Q+Q-1
+    hold the Q tokens of range r, each over the same rows (clipped to its causal prefix)."""
+    B, L, Q = 16, 3000, 3
+    ip = np.arange(B + 1, dtype=np.int32) * L
+    qo = np.arange(B + 1, dtype=np.int32) * Q
+    r = mla.plan_compute_host_multi(qo, ip, 40, causal=True)
+    items, wip = r["items"], r["work_indptr"]
+    assert r["num_ctas"] % Q == 0 and r["num_ctas"] <= 40
+    for rg in range(r["num_ctas"] // Q):
+        per_tok = [[tuple(int(v) for v in x[:3]) for x in items[wip[rg * Q + j]:wip[rg * Q + j + 1]]] for j in range(Q)]
+        for j in range(Q):
+            assert all(int(x[6]) == j for x in items[wip[rg * Q + j]:wip[rg * Q + j + 1]])
+            # same sequences and starts; ends differ only where the causal prefix clips them
+            assert [(b, t0) for b, t0, _ in per_tok[j]] == [(b, t0) for b, t0, _ in per_tok[0]]
+            for (b, t0, t1), (_, _, t1_0) in zip(per_tok[j], per_tok[0]):
+                assert t1 - t1_0 in (0, j) and t1 <= L - Q + j + 1
+    # every query row covered once, in order (the reduce map is checked by the general test)
+    by_row = {}
+    for x in items:
+        by_row.setdefault(int(x[5]), []).append((int(x[1]), int(x[2])))
+    for row, parts in by_row.items():
+        b, j = divmod(row, Q)
+        pos = 0
+        for t0, t1 in parts:
+            assert t0 == pos
+            pos = t1
+        assert pos == L - Q + j + 1
+    # off: each range's tokens back to back in one CTA
+    r2 = mla.plan_compute_host_multi(qo, ip, 40, causal=True, token_parallel=-1)
+    toks = {int(x[6]) for x in r2["items"][r2["work_indptr"][0]:r2["work_indptr"][1]]}
+    assert toks == set(range(Q))
