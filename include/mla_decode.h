@@ -328,10 +328,13 @@ int mla_plan_compute_host_paged(int batch, const int32_t* kv_indptr_host, const 
  * the paged layout above; page_size 1 with kv_last_page_len NULL is plain row
  * addressing.
  *
- * The work is planned per sequence: one CTA processes every query token of a
- * sequence on the same KV rows back to back. The later tokens find the rows in
- * L2 only when the CTAs' ranges fit in it; at B=64, kv_len=8192 they do not, and
- * each token's pass reads the rows from HBM.
+ * When every sequence with KV rows has the same number Q > 1 of query tokens
+ * (the usual speculative-decoding batch), the planner cuts the rows into
+ * ranges for one token and gives each range Q CTAs, one per token, side by
+ * side: they read each row at about the same time, from HBM once and from L2
+ * for the other tokens (option token_parallel). Otherwise one CTA processes the
+ * query tokens of a range back to back on the same rows, which find them in L2
+ * only while the CTAs' ranges fit in it.
  *
  * mla_decode_plan_multi — the planner for that layout (host arrays as for
  *   mla_decode_plan_paged, plus qo_indptr_host [B+1], 0 first, non-decreasing).
