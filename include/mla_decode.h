@@ -228,7 +228,7 @@ int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms,
 
 /*
  * mla_decode_noalloc — the same decode as mla_decode, for callers that cannot
- * allocate device memory. The paper has no counterpart of this entry point.
+ * allocate device memory. None of the cited submissions has such an entry point.
  *
  * Who needs it: code that is handed a stream and its buffers but may not call
  * cudaMalloc — for example a plug-in inside a framework whose caching
