@@ -64,11 +64,13 @@ def test_multi_tokens(mla, mode, k8, causal, layout, split):
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("qn", [2, 4])
 @pytest.mark.parametrize("split", ["whole", "split"])
-def test_multi_tokens_equal_counts(mla, mode, k8, qn, split):
+@pytest.mark.parametrize("layout", ["rows", "pages64"])
+def test_multi_tokens_equal_counts(mla, mode, k8, qn, split, layout):
     # every sequence has qn query tokens: token-parallel plans (one CTA per row range and query
-    # token), whole and split into many ranges
+    # token), whole and split into many ranges, over rows or shuffled pages of 64 (page boxes)
     lengths = [1, 130, 640, 1000, 3 * 128 + 5, 7 * 128, 2000]
-    inp = mi.make_inputs(lengths, mode, seed=320 + mode + qn, permute=True, extra_slots=7)
+    inp = (mi.make_paged_inputs(lengths, 64, mode, seed=320 + mode + qn, permute=True, extra_pages=3)
+           if layout == "pages64" else mi.make_inputs(lengths, mode, seed=320 + mode + qn, permute=True, extra_slots=7))
     # N(0, 1) queries, as on the pages: with a sharper softmax (std 2) fp8's max-abs error on
     # these inputs reaches 0.08-0.11 in any plan (e4m3 P far below the running max loses precision)
     q, qo = mi.make_query_tokens([qn] * len(lengths), seed=330 + qn, q_std=1.0)
