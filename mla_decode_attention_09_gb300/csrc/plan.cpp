@@ -169,7 +169,9 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   auto push = [&](int b, int64_t t0, int64_t t1, int64_t j) {
     items.push_back(WorkItem{b, (int32_t)t0, (int32_t)t1, -1, (int32_t)seq_len(b), (int32_t)(qo[(size_t)b] + j),
                              (int32_t)j, 0});
-    cta_of_item.push_back((int32_t)(token_par ? (int64_t)cta * Qu + j : (int64_t)cta));
+    // token-parallel: token j's CTA of the range. Only a sequence without KV rows can
+    // have more than Qu tokens (its items write zeros); they go to the range's last CTA.
+    cta_of_item.push_back((int32_t)(token_par ? (int64_t)cta * Qu + std::min<int64_t>(j, Qu - 1) : (int64_t)cta));
   };
   for (int b = 0; b < batch; ++b) {
     const int64_t S = tok[(size_t)b], E = tok[(size_t)b + 1], q_b = n_queries(b);
@@ -220,6 +222,8 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
     if (count[(size_t)w.q_row] > 1) w.slot = next[(size_t)w.q_row]++;
 
   // Items are already grouped by CTA in increasing order: CSR offsets.
+  for (int32_t c : cta_of_item)
+    if (c < 0 || (int64_t)c >= used_ctas) return MLA_ERR_ARG;  // not reached: every item has a CTA of the grid
   std::vector<int32_t> indptr((size_t)used_ctas + 1, 0);
   for (size_t i = 0; i < items.size(); ++i) indptr[(size_t)cta_of_item[i] + 1]++;
   for (int64_t c = 0; c < used_ctas; ++c) indptr[(size_t)c + 1] += indptr[(size_t)c];

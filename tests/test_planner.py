@@ -314,3 +314,45 @@ def test_multi_plan_token_parallel():
     r2 = mla.plan_compute_host_multi(qo, ip, 40, causal=True, token_parallel=-1)
     toks = {int(x[6]) for x in r2["items"][r2["work_indptr"][0]:r2["work_indptr"][1]]}
     assert toks == set(range(Q))
+
+
+def test_multi_plan_token_parallel_random():
+    """Token-parallel plans with empty sequences holding other query counts, and equal counts
+    elsewhere: a valid CSR within the grid, every query row produced, causal prefixes covered."""
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        B = int(rng.integers(1, 30))
+        Q = int(rng.choice([2, 3, 4, 8]))
+        lengths = [int(x) for x in rng.integers(0, 2000, B)]
+        q_lens = []
+        for L in lengths:
+            if L == 0 and rng.random() < 0.5:
+                q_lens.append(int(rng.integers(0, 12)))  # an empty sequence may hold any number of tokens
+            else:
+                q_lens.append(Q)
+        if rng.random() < 0.2:
+            lengths[int(rng.integers(0, B))] = 0
+        ip = np.zeros(B + 1, dtype=np.int32)
+        ip[1:] = np.cumsum(lengths)
+        qo = np.zeros(B + 1, dtype=np.int32)
+        qo[1:] = np.cumsum(q_lens)
+        num_sms = int(rng.integers(1, 160))
+        opts = {"min_rows_per_split": 16, "granularity": 16} if rng.random() < 0.5 else {}
+        r = mla.plan_compute_host_multi(qo, ip, num_sms, causal=True, **opts)
+        items, wip = r["items"], r["work_indptr"]
+        assert 1 <= r["num_ctas"] <= max(num_sms, 1) and wip[0] == 0 and wip[-1] == len(items)
+        assert np.all(np.diff(wip) >= 0)
+        by_row = {}
+        for b, t0, t1, slot, L, q_row, q_tok in items:
+            assert L == lengths[b] and q_row == qo[b] + q_tok
+            by_row.setdefault(int(q_row), []).append((int(t0), int(t1)))
+        assert sorted(by_row) == list(range(int(qo[-1])))
+        for b in range(B):
+            for j in range(q_lens[b]):
+                parts = [p for p in by_row[int(qo[b]) + j] if p[1] > p[0]]
+                n = min(max(lengths[b] - q_lens[b] + j + 1, 0), lengths[b])
+                pos = 0
+                for t0, t1 in parts:
+                    assert t0 == pos
+                    pos = t1
+                assert pos == n
