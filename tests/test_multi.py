@@ -81,6 +81,18 @@ def test_multi_tokens_equal_counts(mla, mode, k8, qn, split, layout):
     compare(out, ref, mode, f"equal query counts q={qn} {split}")
 
 
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+def test_multi_tokens_equal_counts_with_empty_sequences(mla, mode, k8):
+    # equal query counts where there are KV rows (a token-parallel plan), and empty sequences
+    # holding other numbers of query tokens, whose outputs are zeros
+    lengths, q_lens = [0, 300, 0, 200, 5], [3, 2, 5, 2, 2]
+    inp = mi.make_inputs(lengths, mode, seed=340 + mode, permute=True, extra_slots=3)
+    q, qo = mi.make_query_tokens(q_lens, seed=341, q_std=1.0)
+    out, plan = run_multi(mla, inp, q, qo, True, num_sms=9, **k8)
+    assert plan.check_error() == 0
+    compare(out, oracle_multi(inp, q, qo, True), mode, "equal counts with empty sequences")
+
+
 def test_multi_query_mismatch_is_reported(mla):
     inp = mi.make_inputs([64, 40], mi.MODE_BF16, seed=8)
     q, qo = mi.make_query_tokens([2, 2], seed=9)
