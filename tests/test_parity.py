@@ -114,6 +114,26 @@ def test_one_very_long_sequence(mla, mode, k8):
 
 
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+def test_degenerate_inputs(mla, mode, k8):
+    # sequence 0: zero query (every score equal: the mean of the value rows); sequence 1: all its
+    # KV rows identical (that row); sequences 2-3: one row each (the row itself); split plans
+    inp = mi.make_inputs([700, 300, 1, 1], mode, seed=600 + mode)
+    inp.q[0] = 0
+    rows = inp.kv_indices[int(inp.kv_indptr[1]):int(inp.kv_indptr[2])].long()
+    inp.kv[rows] = inp.kv[rows[0]].clone()
+    out, plan = run(mla, inp, num_sms=7, min_rows_per_split=16, granularity=16, **k8)
+    assert plan.check_error() == 0
+    ref = oracle_out(inp)
+    compare(out, ref, mode, "degenerate inputs")
+    # the closed forms hold for the oracle's values too (exact up to its float64 rounding)
+    kv = inp.kv.float() if mode == mi.MODE_BF16 else None
+    if kv is not None:
+        r0 = inp.kv_indices[:700].long()
+        assert np.allclose(ref[0], kv[r0, :512].double().mean(0).numpy()[None, :], atol=1e-9)
+        assert np.allclose(ref[1], kv[rows[0], :512].double().numpy()[None, :], atol=1e-9)
+
+
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_peaked_scores(mla, mode, k8):
     # larger query norm -> sharply peaked softmax; exercises the running-max rescale
     inp = mi.make_inputs([300, 1, 77, 2000], mode, seed=9, q_std=6.0)
