@@ -67,3 +67,9 @@ def test_sources_have_no_cpu_fallback():
             if f.endswith((".py", ".cu", ".cpp", ".h", ".cuh")):
                 text = open(os.path.join(dirpath, f), errors="ignore").read()
                 assert "import oracle" not in text and "from oracle" not in text and "liboracle" not in text, f
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    # without the compiled library every entry raises; nothing falls back to a CPU path
+    with pytest.raises(OSError):
+        mla.load_library(str(tmp_path / "libmla_decode.so"))
