@@ -324,10 +324,13 @@ def bench_ours(args):
     barrier(ws)
     torch.cuda.synchronize()
     sampler.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between graph replays: the whole region gives the value, the replays a median
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    e0, e1 = marks[0], torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(reps):
+    for k in range(reps):
         g.replay()
+        marks[k + 1].record()
     if g_tail is not None:
         g_tail.replay()
     e1.record()
@@ -336,6 +339,8 @@ def bench_ours(args):
     barrier(ws)
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, ws, dev)
+    per_call_us = [marks[k].elapsed_time(marks[k + 1]) * 1e3 / chunk for k in range(reps)]
+    median_us = statistics.median(per_call_us) if per_call_us else ms * 1e3 / args.steps
     status = plan.check_error()
     if status != 0:
         raise RuntimeError(f"kernel error status {status}")
@@ -393,6 +398,7 @@ def bench_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "us_per_call": round(ms_per_step * 1e3, 2),
+        "us_per_call_median": round(median_us, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {mi.MODE_BF16: "bf16", mi.MODE_FP8: "e4m3", mi.MODE_A16W8: "f16"}[w.mode], "data": "synthetic",
         "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
