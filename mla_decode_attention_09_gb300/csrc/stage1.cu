@@ -21,12 +21,11 @@
 // that reuses the just-freed stage, with row indices fetched two tiles ahead.
 //
 // fp8 mode: Q is rounded to e4m3 while it is loaded (the pages' direct cast
-// with scale 1), scores use e4m3 x e4m3 mma, and P (scaled by 2^8 so it sits
-// in e4m3's normal range; the factor cancels in O / l) times V uses e4m3 mma
-// as well. The V fragments (four consecutive mma-k rows per register) are
-// assembled from 32-bit shared loads with byte permutes; mma-k is mapped to
-// tile rows as k = 16h + 4c + j -> row 16h + 2c + (j & 1) + 8 (j >> 1), which
-// keeps those loads free of bank conflicts, and P is stored in that k order.
+// with scale 1) and scores use e4m3 x e4m3 mma. P.V runs as f16 m16n8k16
+// mma with P in f16 and every e4m3 value byte converted to f16 exactly (the
+// a16w8 path below): an e4m3 P would keep only 4 significant bits of each
+// weight, too few for a sharply peaked softmax. The V fragments are
+// assembled from 32-bit shared loads with byte permutes.
 //
 // a16w8 mode (bf16 Q x e4m3 KV, the "a16w8" configuration of kernelbot
 // amd-mixed-mla submission 598454 "v12", docstring): f16 m16n8k16 mma. Q is
@@ -42,6 +41,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -72,7 +72,7 @@ struct Cfg<MLA_MODE_FP8> {
   static constexpr int kRowBytes = kQkDim;           // 576
   static constexpr int kRowStride = kRowBytes + 16;  // 592
   static constexpr int kStages = 5;
-  static constexpr int kPStride = kTile + 16;        // e4m3 P row of one head (80 B)
+  static constexpr int kPStride = kTile * 2 + 16;    // f16 P row of one head (144 B)
   static constexpr int kQSteps = kQkDim / 32;        // 18
 };
 template <>
@@ -293,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m_run[2], l_run[2];  // heads g and g+8: running max (base 2) and this thread's partial row sum
   bool timed_out = false;
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const float pofs = (MODE == MLA_MODE_FP8) ? 8.0f : 0.0f;  // P scaled by 2^pofs before rounding
   int tile = 0;
   int parity_item = 0;
 
@@ -394,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha0 = ptx::ex2(m_run[0] - mn0), alpha1 = ptx::ex2(m_run[1] - mn1);
       m_run[0] = mn0;
       m_run[1] = mn1;
-      const float p0 = ptx::ex2(x[0] - mn0 + pofs), p1 = ptx::ex2(x[1] - mn0 + pofs);
-      const float p2 = ptx::ex2(x[2] - mn1 + pofs), p3 = ptx::ex2(x[3] - mn1 + pofs);
+      const float p0 = ptx::ex2(x[0] - mn0), p1 = ptx::ex2(x[1] - mn0);
+      const float p2 = ptx::ex2(x[2] - mn1), p3 = ptx::ex2(x[3] - mn1);
       float ps01, ps23;  // sums of P as rounded for the mma
       if constexpr (MODE == MLA_MODE_BF16) {
         const uint32_t u01 = ptx::pack_bf16x2(p0, p1), u23 = ptx::pack_bf16x2(p2, p3);
@@ -403,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ps23 = __uint_as_float(u23 << 16) + __uint_as_float(u23 & 0xffff0000u);
         *reinterpret_cast<uint32_t*>(pbuf + g * C::kPStride + r0 * 2) = u01;
         *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPStride + r0 * 2) = u23;
-      } else if constexpr (MODE == MLA_MODE_A16W8) {
+      } else {  // fp8 and a16w8: f16 P (P <= 1 against the exact running max)
         const uint32_t u01 = ptx::pack_f16x2(p0, p1), u23 = ptx::pack_f16x2(p2, p3);
         const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&u01));
         const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&u23));
@@ -411,17 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ps23 = f23.x + f23.y;
         *reinterpret_cast<uint32_t*>(pbuf + g * C::kPStride + r0 * 2) = u01;
         *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPStride + r0 * 2) = u23;
-      } else {
-        const uint32_t u01 = ptx::f32x2_to_e4m3x2(p0, p1), u23 = ptx::f32x2_to_e4m3x2(p2, p3);
-        const uint32_t h01 = ptx::e4m3x2_to_f16x2(u01), h23 = ptx::e4m3x2_to_f16x2(u23);
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-        ps01 = f01.x + f01.y;
-        ps23 = f23.x + f23.y;
-        // rows r0, r0+1 sit at mma-k positions 32(w>>2) + 16((w>>1)&1) + 4c + 2(w&1) + {0,1}
-        const int kpos = 32 * (warp >> 2) + 16 * ((warp >> 1) & 1) + 4 * c + 2 * (warp & 1);
-        *reinterpret_cast<uint16_t*>(pbuf + g * C::kPStride + kpos) = (uint16_t)u01;
-        *reinterpret_cast<uint16_t*>(pbuf + (g + 8) * C::kPStride + kpos) = (uint16_t)u23;
       }
       l_run[0] = l_run[0] * alpha0 + ps01;
       l_run[1] = l_run[1] * alpha1 + ps23;
@@ -470,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bb[h][3] = ptx::prmt(t1, t3, 0x7632);
           }
         };
-        if constexpr (MODE == MLA_MODE_A16W8) {
+        {
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {  // 32 rows = two f16 k steps (P in row order)
             uint32_t pa[2][4];
@@ -486,19 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i)
                   ptx::mma_f16_16816(o[4 * blk + i], pa[h], ptx::e4m3x2_to_f16x2(bb[h][i] & 0xffffu),
                                      ptx::e4m3x2_to_f16x2(bb[h][i] >> 16));
-            }
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {  // 32 rows per k step
-            uint32_t pa[4];
-            ptx::ldsm_x4(pa_addr + kk * 32, pa[0], pa[1], pa[2], pa[3]);
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {  // 32 dims: n-tile i column n = dim 64w + 32blk + 4n + i
-              uint32_t bb[2][4];  // b0: mma-k 4c..4c+3 ; b1: 16 + 4c..
-              v_frags(kk, blk, bb);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) ptx::mma_e4m3_16832(o[4 * blk + i], pa, bb[0][i], bb[1][i]);
             }
           }
         }
@@ -580,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (warp == 0 && c == 0) {
         float* pl = p.part_lse + (int64_t)w.slot * kHeads;
-        pl[g] = (L0 > 0.f) ? m_run[0] + __log2f(L0) - pofs : -INFINITY;
-        pl[g + 8] = (L1 > 0.f) ? m_run[1] + __log2f(L1) - pofs : -INFINITY;
+        pl[g] = (L0 > 0.f) ? m_run[0] + __log2f(L0) : -INFINITY;
+        pl[g + 8] = (L1 > 0.f) ? m_run[1] + __log2f(L1) : -INFINITY;
       }
     }
   }
@@ -597,15 +572,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE, bool kPaged>
 int launch_stage1_tp(const DecodeArgs& a, const DevicePlan& p, const uint8_t* zero_row, cudaStream_t stream) {
-  static bool configured[64] = {};  // the shared-memory opt-in is set once per device and instance
+  // the shared-memory opt-in is set once per device and instance (an idempotent
+  // call: threads that race to it both make it, and the flags are atomic)
+  static std::atomic<bool> configured[64] = {};
   const int smem_bytes = Smem<MODE>::kBytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(mla_stage1_kernel<MODE, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return (int)e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.num_ctas <= 0) return 0;
   // programmatic stream serialisation: the prologue may overlap the previous kernel's tail

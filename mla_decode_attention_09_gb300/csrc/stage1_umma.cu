@@ -11,10 +11,12 @@
 //       part 64-byte swizzled, both straight from TMA), B = the e4m3 query
 //       (same layouts), D in TMEM.
 //   softmax over tokens per head (4 warps, one thread per token row),
-//   P^T written to shared memory as [token][16 heads] e4m3,
-//   O^T[512 dims x 16 heads] += V^T[512 x 128] . P^T[128 x 16]
-//       four M = 128 MMAs per 32-token k-step, A = the latent part of the same
-//       tile read MN-major (dims contiguous), B = P^T MN-major, D in TMEM.
+//   P^T written to shared memory as [token][16 heads] e4m3 twice: the
+//       rounded P (hi) and the rounded remainder P - hi (lo),
+//   O^T[512 dims x 32] += V^T[512 x 128] . [P_hi^T | P_lo^T][128 x 32]
+//       four M = 128, N = 32 MMAs per 32-token k-step, A = the latent part of
+//       the same tile read MN-major (dims contiguous), B = both P^T terms
+//       MN-major, D in TMEM; the epilogue adds the hi and lo columns.
 // The value vectors are the first 512 entries of the rows used as keys
 // (kernelbot amd-mixed-mla submission 689529 "MLA decode V3", custom_kernel
 // passes one KV buffer for both), the query is cast directly to e4m3 with
@@ -38,7 +40,7 @@
 // buffered. The producer and the single MMA thread poll their barriers and
 // never block one activity on another. The running max per head is updated lazily:
 // O in TMEM is rescaled only when a tile's max exceeds the reference by more
-// than 2^8, so P = 2^(s - m_ref) <= 256 stays inside e4m3's range.
+// than 2^3, so P = 2^(s - m_ref + 5) <= 256 stays inside e4m3's range.
 //
 // A tile whose 128 rows are consecutive in the KV buffer arrives by TMA as
 // five 2-D box loads. With pages of 16, 32 or 64 rows, a tile that starts
@@ -54,6 +56,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -71,18 +74,31 @@ constexpr int kRopeStage = kRowsU * 64;       // 8 KB: rope part (64-byte rows)
 constexpr int kLatStages = 3, kRopeStages = 2;
 constexpr int kQLat = 4 * 16 * 128;           // 8 KB: e4m3 query latent part, 4 K-blocks x 16 heads x 128 B
 constexpr int kQBytes = kQLat + 16 * 64;      // + 1 KB rope part
-constexpr int kPBuf = kRowsU * 16;            // 2 KB: P^T [128 tokens][16 heads] e4m3
+// P^T of one tile: [128 tokens][16 heads] e4m3 twice, the rounded P (hi) and
+// the rounded remainder P - hi (lo), 2 KB apart: to the P.V MMA they are one
+// B operand of N = 32 columns whose second 16-column group lies kPLo further on.
+constexpr int kPLo = kRowsU * 16;             // 2 KB
+constexpr int kPBuf = 2 * kPLo;               // 4 KB per buffer
 constexpr uint32_t kTileTx = kLatStage + kRopeStage;
 constexpr int kThreadsU = 256;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                 // S^T: 2 buffers x 16 columns
-constexpr uint32_t kColO = 32;                // O^T: 2 buffers x 4 blocks x 16 columns
-constexpr float kTau = 8.0f;
+constexpr uint32_t kColO = 256;               // O^T: 2 buffers x 4 blocks x 32 columns (16 hi + 16 lo)
+// Lazy max: a tile's max is taken (and O rescaled) only when a score exceeds
+// the reference max m_ref by more than kTau (log2 units). P is formed as
+// 2^(s - m_ref + kPShift) <= 2^(kTau + kPShift) = 256, inside e4m3's range
+// (448); the factor 2^kPShift cancels in O / l and is taken out of the LSE. It
+// lifts weights down to 2^-(6 + kPShift) of the reference into e4m3's normal
+// range, where the hi + lo pair keeps ~8 significant bits; a sharp softmax
+// puts most of its weights a few binades below the max.
+constexpr float kTau = 3.0f;
+constexpr float kPShift = 5.0f;
+static_assert(kTau + kPShift <= 8.0f, "P must stay within e4m3's finite range");
 constexpr uint64_t kWaitLimitNsU = 2000000000ull;
 constexpr uint64_t kDrainLimitNsU = 200000000ull;
 constexpr float kLog2eU = 1.4426950408889634f;
 constexpr uint32_t kIdescQK = umma::idesc_e4m3(128, 16, 0, 0);
-constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 16, 1, 1);
+constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 32, 1, 1);
 constexpr uint32_t kLayoutSw64 = 4;
 
 enum : int {
@@ -102,9 +118,10 @@ enum : int {
 struct SU {
   static constexpr int kLat = 0;                                // 3 x 64 KB
   static constexpr int kRope = kLat + kLatStages * kLatStage;   // 2 x 8 KB
-  static constexpr int kQ = kRope + kRopeStages * kRopeStage;   // 9 KB
-  static constexpr int kP = kQ + kQBytes;                       // 2 x 2 KB
-  static constexpr int kRed = kP + 2 * kPBuf;                   // [2][16 heads][4 warps] fp32 tile max
+  // P before the query: every operand the tensor core reads lies well inside the allocation
+  static constexpr int kP = kRope + kRopeStages * kRopeStage;   // 2 x 4 KB
+  static constexpr int kQ = kP + 2 * kPBuf;                     // 9 KB
+  static constexpr int kRed = kQ + kQBytes;                     // [2][16 heads][4 warps] fp32 tile max
   static constexpr int kLsum = kRed + 2 * 64 * 4;               // [16 heads][4 warps] fp32 row sums
   static constexpr int kBar = kLsum + 64 * 4;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
@@ -352,14 +369,16 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   auto issue_pv = [&](const TCur& d, int i) {
     const bool first = d.t0 == d.t_begin;
     const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = p_addr + (i & 1) * kPBuf;
-    const uint32_t ob = tmem + kColO + 64u * (uint32_t)(d.k & 1);
+    const uint32_t ob = tmem + kColO + 128u * (uint32_t)(d.k & 1);
     umma::fence_after_sync();
+    // B = [P_hi^T | P_lo^T], MN-major without swizzle: 8-token core matrices 128 B apart
+    // along K, the lo group kPLo after the hi group along N
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        umma::mma_f8f6f4(ob + 16u * blk, umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
-                         umma::smem_desc(p0 + j * 512, 128, 256, umma::kLayoutNone), kIdescPV,
+        umma::mma_f8f6f4(ob + 32u * blk, umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
+                         umma::smem_desc(p0 + j * 512, 128, kPLo, umma::kLayoutNone), kIdescPV,
                          (first && j == 0) ? 0u : 1u);
     umma::commit(bar(kBPEmpty + (i & 1)));
     umma::commit(bar(kBLEmpty + i % kLatStages));
@@ -748,31 +767,39 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
         continue;
       }
-      float m_ref[16], l[16];
+      // m_s: the reference max per head in log2 units, less kPShift, so that a row's
+      // weight is P = 2^(x - m_s) with x the score in log2 units
+      float m_s[16], l[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
-        m_ref[h] = -INFINITY;
+        m_s[h] = -INFINITY;
         l[h] = 0.f;
       }
       for (int t0 = w.t_begin; t0 < w.t_end; t0 += kRowsU, ++i) {
         const int nv = min(kRowsU, w.t_end - t0);
         // tcgen05.ld is warp-collective: the warp takes the branch together
         bool ok = __all_sync(~0u, wait_u(bar(kBSFull + (i & 1)), (i >> 1) & 1, abort_flag));
-        float x[16];
+        float sr[16];  // raw scores (q8 . k8) of this row for the 16 heads
         if (ok) {
           umma::fence_after_sync();
-          umma::tmem_ld16(tmem + lane_off + kColS + 16u * (uint32_t)(i & 1), x);
+          umma::tmem_ld16(tmem + lane_off + kColS + 16u * (uint32_t)(i & 1), sr);
         }
+        const bool valid = ok && row < nv;
+        // a[h]: exponent of this row's weight against the current reference
+        float a[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) x[h] = (ok && row < nv) ? x[h] * score_log2 : -INFINITY;
-        // Fast path: every score within 2^tau of the reference max needs no
-        // tile max (one barrier ORs the check). A timed-out wait also takes the
-        // full path, whose barrier then stops every thread.
+        for (int h = 0; h < 16; ++h) a[h] = valid ? fmaf(sr[h], score_log2, -m_s[h]) : -INFINITY;
+        // Fast path: every weight at most 2^(kTau + kPShift) needs no tile max
+        // (one barrier ORs the check). A timed-out wait also takes the full
+        // path, whose barrier then stops every thread.
         const bool first = t0 == w.t_begin;
         bool local_need = first || !ok;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) local_need |= x[h] > m_ref[h] + kTau;
+        for (int h = 0; h < 16; ++h) local_need |= a[h] > kTau + kPShift;
         if (ptx::named_bar_or(1, 128, local_need)) {
+          float x[16];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) x[h] = valid ? sr[h] * score_log2 : -INFINITY;
           const float mh = xreduce16<true>(x, lane);
           float* rb = red + (i & 1) * 64;
           if (!(lane & 1)) rb[(lane >> 1) * 4 + warp] = mh;
@@ -780,28 +807,29 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             aborted = true;
             break;
           }
-          float tmax[16], alpha[16];
+          float alpha[16];
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
             const float4 v = *reinterpret_cast<const float4*>(rb + 4 * h);
-            tmax[h] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-            const float mn = fmaxf(m_ref[h], tmax[h]);
-            alpha[h] = ptx::ex2(m_ref[h] - mn);
-            m_ref[h] = mn;
+            const float tmax = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+            const float mn = fmaxf(m_s[h], tmax - kPShift);
+            alpha[h] = ptx::ex2(m_s[h] - mn);
+            m_s[h] = mn;
             l[h] *= alpha[h];
+            a[h] = x[h] - mn;
           }
           if (!first) {  // move the reference up: rescale O once P.V of the previous tile has landed
             const int pt = i - 1;
             if (__all_sync(~0u, wait_u(bar(kBPEmpty + (pt & 1)), (pt >> 1) & 1, abort_flag))) {
               umma::fence_after_sync();
-              const uint32_t ob = tmem + lane_off + kColO + 64u * (uint32_t)(k & 1);
+              const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
 #pragma unroll
-              for (int blk = 0; blk < 4; ++blk) {
+              for (int c16 = 0; c16 < 8; ++c16) {  // 4 blocks x (hi, lo)
                 float o[16];
-                umma::tmem_ld16(ob + 16u * blk, o);
+                umma::tmem_ld16(ob + 16u * c16, o);
 #pragma unroll
                 for (int h = 0; h < 16; ++h) o[h] *= alpha[h];
-                umma::tmem_st16(ob + 16u * blk, o);
+                umma::tmem_st16(ob + 16u * c16, o);
               }
               umma::tmem_wait_st();
             } else {
@@ -809,19 +837,26 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
           }
         }
-        uint32_t pk[4];
+        // P = hi + lo in two e4m3 terms. hi is P rounded to 4 significant bits in
+        // f32 (add half a unit of the 4th bit, clear the bits below), which e4m3
+        // holds exactly in its normal range; lo = P - hi is exact in f32 and
+        // rounded to e4m3 (4 more significant bits). One e4m3 term alone would
+        // keep 4 bits of each weight (relative error up to 2^-4); the pair keeps
+        // about 8. l sums P itself: the MMA's weights differ from it only by the
+        // unbiased rounding of lo (and of hi below e4m3's normal range).
+        uint32_t pk[4], pq[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float p0 = ptx::ex2(x[4 * j] - m_ref[4 * j]), p1 = ptx::ex2(x[4 * j + 1] - m_ref[4 * j + 1]);
-          const float p2 = ptx::ex2(x[4 * j + 2] - m_ref[4 * j + 2]), p3 = ptx::ex2(x[4 * j + 3] - m_ref[4 * j + 3]);
-          pk[j] = ptx::f32x2_to_e4m3x2(p0, p1) | (ptx::f32x2_to_e4m3x2(p2, p3) << 16);
-          const uint32_t h01 = ptx::e4m3x2_to_f16x2(pk[j] & 0xffffu), h23 = ptx::e4m3x2_to_f16x2(pk[j] >> 16);
-          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-          l[4 * j] += f01.x;
-          l[4 * j + 1] += f01.y;
-          l[4 * j + 2] += f23.x;
-          l[4 * j + 3] += f23.y;
+          float pv[4], hv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pv[e] = ptx::ex2(a[4 * j + e]);
+            hv[e] = __uint_as_float((__float_as_uint(pv[e]) + 0x00080000u) & 0xfff00000u);
+            l[4 * j + e] += pv[e];
+          }
+          pk[j] = ptx::f32x2_to_e4m3x2(hv[0], hv[1]) | (ptx::f32x2_to_e4m3x2(hv[2], hv[3]) << 16);
+          pq[j] = ptx::f32x2_to_e4m3x2(pv[0] - hv[0], pv[1] - hv[1]) |
+                  (ptx::f32x2_to_e4m3x2(pv[2] - hv[2], pv[3] - hv[3]) << 16);
         }
         if (ok && row >= nv) {  // row past the item: its value row may hold anything; P.V must see zeros
           uint8_t* vrow = smem + SU::kLat + (i % kLatStages) * kLatStage + row * 128;
@@ -831,8 +866,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(vrow + cb * kBlk + ch * 16) = make_uint4(0, 0, 0, 0);
         }
         if (ok && i >= 2) ok = wait_u(bar(kBPEmpty + (i & 1)), ((i >> 1) - 1) & 1, abort_flag);
-        if (ok)
-          *reinterpret_cast<uint4*>(smem + SU::kP + (i & 1) * kPBuf + row * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        if (ok) {
+          uint8_t* pb = smem + SU::kP + (i & 1) * kPBuf + row * 16;
+          *reinterpret_cast<uint4*>(pb) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(pb + kPLo) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+        }
         umma::fence_proxy_async_smem();
         umma::fence_before_sync();
         umma::mbar_arrive(bar(kBPFull + (i & 1)));
@@ -856,11 +894,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         inv[h] = L[h] > 0.f ? kv_scale / L[h] : 0.f;
       }
       umma::fence_after_sync();
-      const uint32_t ob = tmem + lane_off + kColO + 64u * (uint32_t)(k & 1);
+      const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
-        float o[16];
-        umma::tmem_ld16(ob + 16u * blk, o);
+        float o[16], o_lo[16];
+        umma::tmem_ld16(ob + 32u * blk, o);
+        umma::tmem_ld16(ob + 32u * blk + 16u, o_lo);
+#pragma unroll
+        for (int h = 0; h < 16; ++h) o[h] += o_lo[h];
         const int dcol = 128 * blk + row;
         if (w.slot < 0) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)w.q_row * kHeads * kVDim + dcol;
@@ -875,7 +916,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       if (w.slot >= 0 && tid == 0) {
         float* pl = p.part_lse + (int64_t)w.slot * kHeads;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) pl[h] = L[h] > 0.f ? m_ref[h] + __log2f(L[h]) : -INFINITY;
+        for (int h = 0; h < 16; ++h) pl[h] = L[h] > 0.f ? m_s[h] + __log2f(L[h]) : -INFINITY;
       }
       umma::fence_before_sync();
       umma::mbar_arrive(bar(kBOEmpty + (k & 1)));
@@ -945,11 +986,12 @@ int make_kv_maps(const void* kv, int64_t rows, int page_size, KvMaps* m) {
 }  // namespace
 
 int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* stream) {
-  static bool configured[64] = {};
+  // the shared-memory opt-in, once per device (idempotent; atomic flags)
+  static std::atomic<bool> configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     void* const kernels[4] = {reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<false, false>),
                               reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<false, true>),
                               reinterpret_cast<void*>(mla_stage1_fp8_umma_kernel<true, false>),
@@ -957,7 +999,7 @@ int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* strea
     for (void* k : kernels)
       if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SU::kAlloc);
     if (e != cudaSuccess) return (int)e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.num_ctas <= 0) return 0;
   // rows of the KV pool: the tensor maps' second extent; one past it reads as zeros

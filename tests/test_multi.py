@@ -71,9 +71,8 @@ def test_multi_tokens_equal_counts(mla, mode, k8, qn, split, layout):
     lengths = [1, 130, 640, 1000, 3 * 128 + 5, 7 * 128, 2000]
     inp = (mi.make_paged_inputs(lengths, 64, mode, seed=320 + mode + qn, permute=True, extra_pages=3)
            if layout == "pages64" else mi.make_inputs(lengths, mode, seed=320 + mode + qn, permute=True, extra_slots=7))
-    # N(0, 1) queries, as on the pages: with a sharper softmax (std 2) fp8's max-abs error on
-    # these inputs reaches 0.08-0.11 in any plan (e4m3 P far below the running max loses precision)
-    q, qo = mi.make_query_tokens([qn] * len(lengths), seed=330 + qn, q_std=1.0)
+    # queries of std 2: a sharper softmax than N(0, 1), where each weight's rounding in P.V shows
+    q, qo = mi.make_query_tokens([qn] * len(lengths), seed=330 + qn, q_std=2.0)
     opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
     out, plan = run_multi(mla, inp, q, qo, True, num_sms=152 if split == "whole" else 12, **k8, **opts)
     assert plan.check_error() == 0
@@ -115,8 +114,5 @@ def test_multi_full_size(mla, k8):
     q, qo = mi.make_query_tokens([2] * 64, seed=91)
     out, plan = run_multi(mla, inp, q, qo, True, **k8)
     assert plan.check_error() == 0
-    seqs = [0, 33, 63]
-    rows = [int(qo[b]) + j for b in seqs for j in range(2)]
-    ref_all = oracle_multi(inp, q, qo, True)
-    compare(out[rows], ref_all[rows], mi.MODE_FP8, "multi full size")
-    assert torch.isfinite(out.float()).all()
+    # every query row, element by element
+    compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, "multi full size")

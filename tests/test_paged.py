@@ -141,6 +141,5 @@ def test_paged_full_size(mla, order):
     inp = mi.make_paged_inputs(lengths, 8, mi.MODE_FP8, seed=77, permute=order == "shuffled")
     out, plan = run_paged(mla, inp)
     assert plan.check_error() == 0
-    ids = [0, 17, 40, 63]
-    compare(out[ids], oracle_paged(inp, seq_ids=ids), mi.MODE_FP8, f"paged full size {order}")
-    assert torch.isfinite(out.float()).all()
+    # every sequence, element by element
+    compare(out, oracle_paged(inp), mi.MODE_FP8, f"paged full size {order}")
