@@ -257,9 +257,16 @@ int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms,
  *                  (MLA_ERR_TIMEOUT, MLA_ERR_PLAN_MISMATCH, MLA_ERR_INDEX).
  * The first call on a device does a one-time set-up: it resolves the array's
  * device address and clears part of it, and synchronises the device. Make that
- * first call before any stream capture. Every call reuses the same array, which
- * keeps the last call's contents: calls whose device work overlaps (on
- * different streams, or unordered) race on it and corrupt each other's results.
+ * first call before any stream capture; while `stream` is being captured the
+ * set-up is not attempted (MLA_ERR_CUDA), and a set-up that failed is retried
+ * by the next call. Every call reuses the same array, which keeps the last
+ * call's contents: calls whose device work overlaps (on different streams, or
+ * unordered) race on it and corrupt each other's results.
+ * Host costs: each call plans into about 93 KB of the calling thread's stack
+ * (give threads with small stacks room for it), and uploads the work list
+ * (up to about 90 KB) with cudaMemcpyAsync from that pageable memory, which the
+ * runtime stages before returning and which can make the call wait for work
+ * queued earlier on the stream.
  * Errors returned directly: MLA_ERR_ARG, MLA_ERR_DTYPE, MLA_ERR_ALIGN,
  * MLA_ERR_INDPTR, MLA_ERR_DEVICE, MLA_ERR_CUDA, MLA_ERR_NOALLOC_LIMIT.
  */

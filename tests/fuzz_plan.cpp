@@ -1,12 +1,67 @@
 // Random inputs for the host split-KV planners (row, paged and multi-token
-// layouts, extreme options). Built with -fsanitize=address,undefined by
-// tests/test_planner_fuzz.py; checks the work list, CSR and reduce map.
+// layouts, extreme options, and the fixed-capacity planner of
+// mla_decode_noalloc). Built with -fsanitize=address,undefined by
+// tests/test_planner_fuzz.py; checks the work list, CSR and reduce map, and
+// that the row-layout plans cover every row of every sequence exactly once.
 #include <cstdio>
 #include <cstdlib>
+#include <memory>
 #include <random>
 #include <vector>
 #include "internal.h"
+#include "noalloc_plan.h"
 using namespace mla;
+
+// Row-layout plan check: the items of each sequence are consecutive, in CTA
+// order, and cover [0, L_b) exactly once from the start; an empty sequence has
+// one empty item; a sequence of several items owns one reduce entry whose
+// consecutive slots the items take in order, a one-item sequence writes its
+// output directly (slot -1). Returns an error message or nullptr.
+static const char* check_rows(int B, const int32_t* ip, const WorkItem* items, int n_items, const int32_t* indptr,
+                              int n_ctas, const ReduceEntry* red, int n_reduce, int n_slots) {
+  if (n_ctas < 1 || indptr[0] != 0 || indptr[n_ctas] != n_items) return "csr ends";
+  for (int c = 0; c < n_ctas; ++c)
+    if (indptr[c + 1] < indptr[c]) return "csr order";
+  std::vector<int> red_of(B, -1);
+  for (int r = 0; r < n_reduce; ++r) {
+    if (red[r].b < 0 || red[r].b >= B || red_of[red[r].b] >= 0) return "reduce entry";
+    if (red[r].slot_begin < 0 || red[r].n_slots < 2 || red[r].slot_begin + red[r].n_slots > n_slots)
+      return "reduce slots";
+    red_of[red[r].b] = r;
+  }
+  int i = 0, prev_b = -1;
+  while (i < n_items) {
+    const int b = items[i].b;
+    if (b <= prev_b || b >= B) return "sequence order";
+    int j = i;
+    int32_t t = 0;
+    const int32_t L = ip[b + 1] - ip[b];
+    while (j < n_items && items[j].b == b) {
+      const WorkItem& w = items[j];
+      if (w.t_begin != t || w.t_end < w.t_begin || w.seq_len != L || w.q_row != b || w.q_tok != 0) return "item";
+      if (w.t_end == w.t_begin && L > 0) return "empty item";
+      t = w.t_end;
+      ++j;
+    }
+    if (t != L) return "coverage";
+    if (j - i == 1) {
+      if (items[i].slot != -1 || red_of[b] >= 0) return "whole sequence slot";
+    } else {
+      const int r = red_of[b];
+      if (r < 0 || red[r].n_slots != j - i) return "split sequence reduce";
+      for (int k = i; k < j; ++k)
+        if (items[k].slot != red[r].slot_begin + (k - i)) return "slot order";
+    }
+    prev_b = b;
+    i = j;
+  }
+  if (prev_b != B - 1 && B > 0) {
+    // every sequence must appear
+    return "missing sequence";
+  }
+  return nullptr;
+}
+
 int main(int argc, char** argv) {
   std::mt19937_64 rng(argc > 1 ? atoll(argv[1]) : 1);
   auto U = [&](int64_t lo, int64_t hi) { return (int64_t)(lo + rng() % (uint64_t)(hi - lo + 1)); };
@@ -49,8 +104,50 @@ int main(int argc, char** argv) {
     }
     for (int r = 0; r < h.n_reduce; ++r)
       if (h.reduce[r].slot_begin < 0 || h.reduce[r].slot_begin + h.reduce[r].n_slots > h.num_slots) { printf("bad reduce\n"); return 1; }
+    if (kind == 0) {
+      const char* e = check_rows(B, ip.data(), h.items, h.n_items, h.work_indptr, h.num_ctas, h.reduce, h.n_reduce,
+                                 h.num_slots);
+      if (e) { printf("row plan: %s (iter %d)\n", e, iter); return 1; }
+    }
     free_host_plan(&h);
   }
-  printf("ok %d err %d\n", ok, err);
+
+  // The fixed-capacity planner of mla_decode_noalloc: up to its batch limit,
+  // lengths from empty to long, any SM count.
+  auto fp = std::make_unique<noalloc::FixedPlan>();
+  int fixed_ok = 0, fixed_limit = 0;
+  for (int iter = 0; iter < iters / 4; ++iter) {
+    const int B = (int)(U(0, 3) == 0 ? U(0, noalloc::kMaxBatch) : U(0, 70));
+    const int num_sms = (int)std::vector<int64_t>{1, 2, 7, 148, 152, 1024, 5000}[U(0, 6)];
+    const int64_t max_len = std::vector<int64_t>{1, 200, 9000, 300000}[U(0, 3)];
+    std::vector<int32_t> ip(B + 1, 0);
+    for (int b = 0; b < B; ++b) ip[b + 1] = ip[b] + (int32_t)(U(0, 4) == 0 ? 0 : U(0, max_len));
+    const int rc = noalloc::plan_fixed(B, ip.data(), num_sms, fp.get());
+    if (rc == MLA_ERR_NOALLOC_LIMIT) { ++fixed_limit; continue; }
+    if (rc != MLA_OK) { printf("fixed plan: rc %d\n", rc); return 1; }
+    ++fixed_ok;
+    if (B == 0) continue;
+    if (fp->n_ctas > std::min(num_sms, noalloc::kMaxCtas)) { printf("fixed plan: %d ctas\n", fp->n_ctas); return 1; }
+    if (fp->n_items > noalloc::kMaxItems || fp->n_slots > noalloc::kMaxSlots || fp->n_reduce > noalloc::kMaxReduce) {
+      printf("fixed plan: capacity\n");
+      return 1;
+    }
+    const char* e = check_rows(B, ip.data(), fp->items, fp->n_items, fp->indptr, fp->n_ctas, fp->reduce,
+                               fp->n_reduce, fp->n_slots);
+    if (e) { printf("fixed plan: %s (iter %d, B %d, sms %d)\n", e, iter, B, num_sms); return 1; }
+    // balance: no CTA holds more than the even share of 128-row granules, rounded up,
+    // and at least one 128-row granule when there are rows
+    int64_t granules = 0;
+    for (int b = 0; b < B; ++b) granules += (ip[b + 1] - ip[b] + 127) / 128;
+    const int64_t share = std::max<int64_t>(1, (granules + std::min(num_sms, noalloc::kMaxCtas) - 1) /
+                                                   std::min(num_sms, noalloc::kMaxCtas));
+    for (int c = 0; c < fp->n_ctas; ++c) {
+      int64_t g = 0;
+      for (int i = fp->indptr[c]; i < fp->indptr[c + 1]; ++i)
+        g += (fp->items[i].t_end - fp->items[i].t_begin + 127) / 128;
+      if (g > share + 1) { printf("fixed plan: cta %d holds %lld granules, share %lld\n", c, (long long)g, (long long)share); return 1; }
+    }
+  }
+  printf("ok %d err %d fixed %d limit %d\n", ok, err, fixed_ok, fixed_limit);
   return 0;
 }

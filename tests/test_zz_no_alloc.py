@@ -4,8 +4,9 @@ allocator already holds the GPU's memory, or a serving loop that cannot afford
 cudaMalloc's implicit synchronisation. Instead of a plan's workspace it keeps
 its work list and partial results in a fixed array inside the library.
 
-Its output must match the regular mla_decode (with a planned workspace) within
-the parity tolerances, on two calls in a row that reuse the same fixed array.
+Its output must match the regular mla_decode (with a planned workspace) and
+the float64 oracle within the parity tolerances, on two calls in a row that
+reuse the same fixed array.
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it also passes alone in a fresh process.
 """
@@ -16,6 +17,7 @@ import pytest
 import torch
 
 import mla_inputs as mi
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +67,8 @@ def test_noalloc_matches_planned_decode_twice(mla, mode, lengths):
     ref = mla.decode(d.q, d.kv, ks, d.kv_indptr, d.kv_indices, sm_scale=inp.sm_scale, dtype_mode=mode, plan=plan)
     assert plan.check_error() == 0
 
+    expect, _ = oracle.decode(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, inp.sm_scale, mode, inp.kv_scale)
+
     lib = mla.load_library()
     status = torch.full((1,), 123, dtype=torch.int32, device="cuda")
     for _ in range(2):  # the second call reuses whatever the first left in the fixed array
@@ -73,6 +77,7 @@ def test_noalloc_matches_planned_decode_twice(mla, mode, lengths):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         _close(out, ref, mode)
+        _close(out, torch.from_numpy(expect), mode)
 
 
 def test_noalloc_rejects_oversized_requests(mla):
