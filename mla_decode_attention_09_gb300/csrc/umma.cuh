@@ -1,7 +1,7 @@
 // Inline-PTX wrappers for the 5th-generation tensor core path of sm_103a:
 // TMEM allocation, tcgen05.mma (kind::f8f6f4) with shared-memory matrix
 // descriptors, tcgen05.commit to mbarriers, TMEM loads/stores, TMA tensor
-// loads (tiled and 4-row gather) and 16-byte cp.async row copies.
+// loads and 16-byte cp.async row copies.
 #pragma once
 
 #include <cuda.h>
@@ -101,16 +101,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
-// Four rows y0..y3 (each one box row wide, starting at column x) into four consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y0, int32_t y1,
-                                            int32_t y2, int32_t y3, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
-      "[%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 // Warm L2 with one tiled box (no shared memory involved).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(reinterpret_cast<uint64_t>(tm)),
