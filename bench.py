@@ -82,15 +82,20 @@ def max_over_ranks(x: float, ws: int, device) -> float:
 # ---------------------------------------------------------------- clocks (NVML, read only)
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons of one GPU in a thread (NVML via ctypes)."""
+    """Samples SM clock and clock-event reasons of one GPU in a thread (NVML via ctypes).
+
+    Each sample carries the region that was marked when it was taken (mark(name)
+    before a region, mark(None) after it), so a summary can cover the samples
+    taken inside one timed region."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting",
                0x1: "gpu_idle", 0x10: "sync_boost", 0x100: "display_clock_setting"}
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, period_s: float = 0.0005):
         self.period = period_s
-        self.samples = []
+        self.samples = []  # (region, sm_mhz, reasons)
+        self.region = None
         self.max_mhz = None
         self._stop = threading.Event()
         self._thread = None
@@ -127,12 +132,17 @@ class ClockSampler:
         fn(self.handle, ctypes.byref(rs))
         return int(clk.value), int(rs.value)
 
+    def _sample(self):
+        try:
+            region = self.region
+            mhz, reasons = self._read()
+            self.samples.append((region, mhz, reasons))
+        except Exception:
+            pass
+
     def _loop(self):
         while not self._stop.is_set():
-            try:
-                self.samples.append(self._read())
-            except Exception:
-                pass
+            self._sample()
             time.sleep(self.period)
 
     def start(self):
@@ -140,26 +150,34 @@ class ClockSampler:
             self._thread = threading.Thread(target=self._loop, daemon=True)
             self._thread.start()
 
+    def mark(self, region):
+        """Enter (name) or leave (None) a region; a sample is taken at each mark."""
+        if self.nvml is not None:
+            if region is None:
+                self._sample()
+            self.region = region
+            if region is not None:
+                self._sample()
+
     def stop(self):
         if self._thread is not None:
             self._stop.set()
             self._thread.join()
-            try:
-                self.samples.append(self._read())
-            except Exception:
-                pass
 
-    def summary(self) -> dict:
-        if not self.samples:
+    def summary(self, region) -> dict:
+        """Clocks over the samples of one region (None: every sample taken inside any region)."""
+        sel = [x for x in self.samples if (x[0] == region if region is not None else x[0] is not None)]
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
                     "source": "nvml", "note": self.error or "no samples"}
-        mhz = [s[0] for s in self.samples]
+        mhz = [x[1] for x in sel]
         mask = 0
-        for _, r in self.samples:
-            mask |= r
+        for x in sel:
+            mask |= x[2]
         reasons = [name for bit, name in self.REASONS.items() if mask & bit and name != "gpu_idle"]
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
-                "samples": len(mhz), "source": "nvml"}
+        return {"sm_mhz": statistics.median(mhz), "sm_min_mhz": min(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(mhz), "period_ms": self.period * 1e3,
+                "region": region or "every timed region", "source": "nvml"}
 
 
 # ---------------------------------------------------------------- helpers
@@ -230,6 +248,79 @@ def parse_layout(text: str):
     raise SystemExit(f"bad --layout {text!r}: rows, rows:shuffled, pages:N or pages:N:shuffled")
 
 
+def l2_bytes(dev) -> int:
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20)
+
+
+def copies_for(bytes_per_copy: int, dev) -> int:
+    """Input copies rotated call after call so that no call finds its inputs in L2:
+    two when one copy exceeds L2, else enough that the copies span three L2s."""
+    l2 = l2_bytes(dev)
+    if bytes_per_copy > l2:
+        return 2
+    return max(2, -(-3 * l2 // max(bytes_per_copy, 1)))
+
+
+class GraphTimer:
+    """K calls of `call(k)` (k = call index) captured in CUDA graphs of `chunk`
+    calls each and replayed; CUDA events between replays on the replay stream."""
+
+    def __init__(self, call, steps: int, chunk: int):
+        self.steps = steps
+        self.chunk = max(1, min(chunk, steps))
+        reps, tail = divmod(steps, self.chunk)
+        self.reps = reps
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        self.graphs = []
+        for n in ([self.chunk] if reps else []) + ([tail] if tail else []):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for k in range(n):
+                        call(k)
+            self.graphs.append(g)
+        torch.cuda.current_stream().wait_stream(s)
+        self.tail = self.graphs[-1] if tail else None
+        self.main = self.graphs[0] if reps else None
+        for g in self.graphs:  # one untimed replay of each graph
+            g.replay()
+        torch.cuda.synchronize()
+
+    def run(self):
+        """Returns (total ms, median µs per call over the full replays)."""
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(self.reps + 1)]
+        e1 = torch.cuda.Event(enable_timing=True)
+        marks[0].record()
+        for k in range(self.reps):
+            self.main.replay()
+            marks[k + 1].record()
+        if self.tail is not None:
+            self.tail.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = marks[0].elapsed_time(e1)
+        per = [marks[k].elapsed_time(marks[k + 1]) * 1e3 / self.chunk for k in range(self.reps)]
+        return ms, (statistics.median(per) if per else ms * 1e3 / self.steps)
+
+
+def time_stage1_graph(mla, devs, scales, outs, plan, mode, calls: int) -> float:
+    """µs per stage-1 launch, timed the way the decode call runs it: consecutive
+    stage-1-only launches (each with the programmatic-serialisation attribute the
+    decode uses) in a CUDA graph, rotating through the input copies."""
+    n = len(devs)
+
+    def call(k):
+        d = devs[k % n]
+        mla.decode_stage1(d.q, d.kv, scales[k % n], d.kv_indptr, d.kv_indices, outs[k % n], plan=plan,
+                          sm_scale=d.sm_scale, dtype_mode=mode)
+
+    chunk = n * max(1, 64 // n)
+    t = GraphTimer(call, max(calls, chunk), chunk)
+    ms, _ = t.run()
+    return ms * 1e3 / t.steps
+
+
 def bench_ours(args):
     import mla_decode_attention_09_gb300 as mla
     from mla_decode_attention_09_gb300 import build as mla_build
@@ -246,8 +337,12 @@ def bench_ours(args):
     default_layout = kind == "rows" and not shuffled and q_len == 1
     # algorithmic bytes: KV rows read once, Q read and O written for every query token
     step_bytes = nbytes["kv"] + (nbytes["q"] + nbytes["o"]) * q_len
+    peak, peak_kind = measured_peak()
 
-    # two input copies, each larger than L2 for the headline workload (seeded per rank: independent replicas)
+    # input copies rotated call after call, none found in L2 by the next call that uses it
+    # (seeded per rank: independent replicas)
+    n_copies = copies_for(step_bytes, dev)
+
     def make(k):
         seed = w.seed + replica_seed_offset(rank, k)
         lens = mi.workload_lengths(w)
@@ -257,14 +352,14 @@ def bench_ours(args):
             return mi.make_inputs(lens, w.mode, seed, permute=True, device=str(dev))
         return mi.make_workload(w, device=str(dev), seed_offset=replica_seed_offset(rank, k))
 
-    devs = [make(k) for k in range(2)]
+    devs = [make(k) for k in range(n_copies)]
     scales = [d.kv_scale_tensor(dev) for d in devs]
     opts = {"num_kv_slots": devs[0].kv.shape[0], "fp8_kernel": args.fp8_kernel}
     last_host = devs[0].kv_last_page_len.cpu() if kind == "pages" else None
     queries = None
     if q_len > 1:
         queries = []
-        for k in range(2):
+        for k in range(n_copies):
             qh, qo = mi.make_query_tokens([q_len] * w.batch, seed=w.seed + 50 + replica_seed_offset(rank, k))
             queries.append((qh.to(dev), qo.to(dev)))
         plan = mla.plan_multi(queries[0][1].cpu(), devs[0].kv_indptr.cpu(), causal=True, page_size=page_size,
@@ -274,9 +369,10 @@ def bench_ours(args):
     else:
         plan = mla.plan(devs[0].kv_indptr.cpu(), 0, **opts)
     info = plan.info()
-    outs = [torch.empty((w.batch * q_len, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    outs = [torch.empty((w.batch * q_len, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(n_copies)]
 
     def call(k, stream=None):
+        k %= n_copies
         d = devs[k]
         if queries is not None:
             mla.decode_multi(queries[k][0], d.kv, scales[k], queries[k][1], d.kv_indptr, d.kv_indices, outs[k],
@@ -290,57 +386,23 @@ def bench_ours(args):
                        dtype_mode=w.mode, plan=plan, stream=stream, validate=False)
 
     for k in range(max(args.warmup, 3)):
-        call(k % 2)
+        call(k)
     torch.cuda.synchronize()
     status = plan.check_error()
     if status != 0:
         raise RuntimeError(f"kernel error status {status}")
 
-    # CUDA graph with `chunk` decode calls (alternating copies), replayed to cover K steps
-    chunk = min(args.steps, 64)
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            for k in range(chunk):
-                call(k % 2)
-    torch.cuda.current_stream().wait_stream(s)
-    g.replay()
-    torch.cuda.synchronize()
-    reps, tail = divmod(args.steps, chunk)
-    g_tail = None
-    if tail:
-        g_tail = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g_tail, stream=s):
-                for k in range(tail):
-                    call(k % 2)
-        torch.cuda.current_stream().wait_stream(s)
-        g_tail.replay()
-        torch.cuda.synchronize()
-
-    sampler = ClockSampler(local)
-    barrier(ws)
-    torch.cuda.synchronize()
+    # exactly K decode calls in CUDA graphs (chunks of 64 calls, rotating the copies)
+    timer = GraphTimer(call, args.steps, n_copies * max(1, 64 // n_copies))
+    sampler = ClockSampler(local, period_s=args.clock_period_ms * 1e-3)
     sampler.start()
-    # one event between graph replays: the whole region gives the value, the replays a median
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    e0, e1 = marks[0], torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for k in range(reps):
-        g.replay()
-        marks[k + 1].record()
-    if g_tail is not None:
-        g_tail.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    sampler.stop()
     barrier(ws)
-    ms = e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    sampler.mark("timed")
+    ms, median_us = timer.run()
+    sampler.mark(None)
+    barrier(ws)
     ms_max = max_over_ranks(ms, ws, dev)
-    per_call_us = [marks[k].elapsed_time(marks[k + 1]) * 1e3 / chunk for k in range(reps)]
-    median_us = statistics.median(per_call_us) if per_call_us else ms * 1e3 / args.steps
     status = plan.check_error()
     if status != 0:
         raise RuntimeError(f"kernel error status {status}")
@@ -348,28 +410,17 @@ def bench_ours(args):
     value = whole_job_gbs(step_bytes, args.steps, ws, ms_max)
     launches_per_step = 1 + (1 if info["num_split_seqs"] > 0 else 0)
 
-    # roofline of the dominant kernel: stage 1 alone, each launch bracketed by events on its stream
-    # (the row layout has a stage-1-only entry point; other layouts bracket the whole call)
-    n_roof = max(8, min(args.steps, 200))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_roof)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(200_000_000)  # keep the GPU busy while the launches below are queued: no host gaps
+    # roofline of the dominant kernel, stage 1, timed as the call runs it (a graph of
+    # consecutive stage-1 launches); other layouts than rows with one query token have no
+    # stage-1-only entry point and report the whole call
     stage1_only = kind == "rows" and q_len == 1
-    for i in range(n_roof):
-        d = devs[i % 2]
-        ev[i][0].record()
-        if stage1_only:
-            mla.decode_stage1(d.q, d.kv, scales[i % 2], d.kv_indptr, d.kv_indices, outs[i % 2], plan=plan,
-                              sm_scale=d.sm_scale, dtype_mode=w.mode)
-        else:
-            call(i % 2)
-        ev[i][1].record()
-        if stage1_only:
-            mla.decode_reduce(outs[i % 2], plan=plan)
-    torch.cuda.synchronize()
-    stage1_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    peak, peak_kind = measured_peak()
-    achieved = step_bytes / (stage1_ms * 1e-3) / 1e9
+    sampler.mark("roofline")
+    if stage1_only:
+        kern_us = time_stage1_graph(mla, devs, scales, outs, plan, w.mode, args.roofline_calls)
+    else:
+        kern_us = ms_per_step * 1e3
+    sampler.mark(None)
+    achieved = step_bytes / (kern_us * 1e-6) / 1e9
     kernel = ("mla_stage1_fp8_umma_kernel" if (w.mode == mi.MODE_FP8 and args.fp8_kernel == 0)
               else "mla_stage1_kernel")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -377,16 +428,29 @@ def bench_ours(args):
                 "traffic": ncu_traffic(kernel, args.workload) if default_layout else None,
                 "kernel": kernel, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": step_bytes,
-                "stage1_us" if stage1_only else "call_us": round(stage1_ms * 1e3, 2)}
+                "stage1_us" if stage1_only else "call_us": round(kern_us, 2),
+                "call_us": round(ms_per_step * 1e3, 2),
+                "call_frac": round(value / ws / peak, 4),
+                "timing": ("CUDA graph of consecutive stage-1 launches with the decode's launch attribute"
+                           if stage1_only else "the whole decode call")}
 
     # end to end and the oracle baseline are measured on the row layout with one query token
     e2e = None
     if not args.no_e2e and default_layout:
         e2e = bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes)
     assert plan.check_error() == 0
+
+    per_config = None
+    if rank == 0 and default_layout and not args.no_per_config:
+        sampler.mark("per_config")
+        per_config = bench_per_config(mla, dev, args, peak, current=(args.workload, ms_per_step * 1e3, median_us,
+                                                                     kern_us if stage1_only else None, n_copies))
+        sampler.mark(None)
+    sampler.stop()
+
     host0 = (devs[0].to("cpu") if (rank == 0 and ws == 1 and not args.no_cpu_baseline and default_layout)
              else None)
-
+    del devs, outs
     cpu = None
     if host0 is not None:
         n_seq = args.cpu_sample_seqs
@@ -394,7 +458,8 @@ def bench_ours(args):
         cpu = {"value": round(cbytes / secs / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"float64 oracle on {min(n_seq, w.batch)} of {w.batch} sequences ({secs:.1f} s)"}
 
-    clocks = sampler.summary()
+    clocks = sampler.summary("timed")
+    clocks["all_regions"] = sampler.summary(None)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "us_per_call": round(ms_per_step * 1e3, 2),
@@ -405,19 +470,63 @@ def bench_ours(args):
                    "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": page_size,
                    "kv_order": "shuffled" if shuffled else ("workload" if kind == "rows" else "in order"),
                    "q_len": q_len, "causal": q_len > 1, "bytes_per_call": step_bytes,
-                   "l2": "inputs larger than L2, two copies alternate", "timing": "CUDA graphs of decode calls",
+                   "l2": (f"{n_copies} input copies rotate call after call "
+                          + ("(each larger than L2)" if n_copies == 2 and step_bytes > l2_bytes(dev)
+                             else "(together three times L2)")),
+                   "timing": "CUDA graphs of decode calls",
                    "plan": {k: info[k] for k in ("num_ctas", "num_work_items", "num_split_seqs")},
                    "fp8_kernel": ("tcgen05" if args.fp8_kernel == 0 else "mma.sync") if w.mode == mi.MODE_FP8 else None},
         "frac_of_peak": round(value / ws / peak, 4), "peak_gbs": peak,
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "roofline": roofline, "per_config": per_config, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
-    if args.all_workloads and rank == 0 and default_layout:
-        line["per_workload"] = per_workload(mla, dev, fp8_kernel=args.fp8_kernel)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def bench_per_config(mla, dev, args, peak, current, calls: int = 1000):
+    """Every workload of the five, timed like the headline: CUDA graphs of decode calls
+    that rotate through enough input copies that none is found in L2, then stage 1 alone
+    in a graph of consecutive stage-1 launches. `current` carries the headline's own
+    measurement (workload, µs per call, median, stage-1 µs, copies), reused for that row."""
+    res = {}
+    for name, w in mi.WORKLOADS.items():
+        nb = mi.workload_bytes(w)["total"]
+        if name == current[0]:
+            us, med, s1, n_copies = current[1], current[2], current[3], current[4]
+        else:
+            n_copies = copies_for(nb, dev)
+            devs = [mi.make_workload(w, device=str(dev), seed_offset=k) for k in range(n_copies)]
+            scales = [d.kv_scale_tensor(dev) for d in devs]
+            plan = mla.plan(devs[0].kv_indptr.cpu(), 0, num_kv_slots=devs[0].kv.shape[0], fp8_kernel=args.fp8_kernel)
+            outs = [torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(n_copies)]
+
+            def call(k):
+                d = devs[k % n_copies]
+                mla.decode(d.q, d.kv, scales[k % n_copies], d.kv_indptr, d.kv_indices, outs[k % n_copies],
+                           sm_scale=d.sm_scale, dtype_mode=w.mode, plan=plan, validate=False)
+
+            for k in range(3):
+                call(k)
+            torch.cuda.synchronize()
+            assert plan.check_error() == 0
+            chunk = n_copies * max(1, 64 // n_copies)
+            t = GraphTimer(call, max(calls, chunk), chunk)
+            ms, med = t.run()
+            us = ms * 1e3 / t.steps
+            s1 = time_stage1_graph(mla, devs, scales, outs, plan, w.mode, max(calls, chunk))
+            assert plan.check_error() == 0
+            del devs, outs, plan
+        res[name] = {"desc": w.describe(), "us_per_call": round(us, 2), "us_per_call_median": round(med, 2),
+                     "gbs": round(nb / (us * 1e-6) / 1e9, 1), "frac": round(nb / (us * 1e-6) / 1e9 / peak, 4),
+                     "stage1_us": round(s1, 2) if s1 is not None else None,
+                     "stage1_frac": round(nb / (s1 * 1e-6) / 1e9 / peak, 4) if s1 else None,
+                     "bytes": nb, "copies": n_copies}
+    res["method"] = ("CUDA graphs of decode calls rotating through input copies (two when one copy exceeds L2, "
+                     "else enough to span three L2s); stage 1 alone as a graph of consecutive stage-1 launches")
+    return res
 
 
 def bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes):
@@ -459,41 +568,6 @@ def bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
            "note": "all inputs (q, KV cache, indices, scale) copied from pinned host memory every step"}
     return e2e
-
-
-def per_workload(mla, dev, calls: int = 200, fp8_kernel: int = 0):
-    """µs/call and GB/s of every workload, one call at a time with a cold L2: a
-    512 MB read between timed calls leaves L2 full of clean unrelated lines (a
-    scrub write would leave dirty lines that the timed call must write back)."""
-    res = {}
-    scrub = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty((), dtype=torch.float32, device=dev)
-    for name, w in mi.WORKLOADS.items():
-        inp = mi.make_workload(w, device=str(dev))
-        ks = inp.kv_scale_tensor(dev)
-        plan = mla.plan(inp.kv_indptr.cpu(), 0, num_kv_slots=inp.kv.shape[0], fp8_kernel=fp8_kernel)
-        out = torch.empty((w.batch, 16, 512), dtype=torch.bfloat16, device=dev)
-        torch.cuda._sleep(100_000_000)
-        for _ in range(5):
-            mla.decode(inp.q, inp.kv, ks, inp.kv_indptr, inp.kv_indices, out, sm_scale=inp.sm_scale,
-                       dtype_mode=w.mode, plan=plan, validate=False)
-        times = []
-        for _ in range(calls):
-            torch.sum(scrub, dim=0, out=sink)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            mla.decode(inp.q, inp.kv, ks, inp.kv_indptr, inp.kv_indices, out, sm_scale=inp.sm_scale,
-                       dtype_mode=w.mode, plan=plan, validate=False)
-            b.record()
-            times.append((a, b))
-        torch.cuda.synchronize()
-        us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3
-        nb = mi.workload_bytes(w)["total"]
-        res[name] = {"us_per_call": round(us, 2), "gbs": round(nb / (us * 1e-6) / 1e9, 1),
-                     "bytes": nb, "l2": "cold (512 MB read before each call)"}
-        assert plan.check_error() == 0
-        del inp, out, plan
-    return res
 
 
 # ---------------------------------------------------------------- reference arm (the oracle on host cores)
@@ -548,7 +622,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="fp8_b64_l8192", choices=list(mi.WORKLOADS) + list(mi.EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--all-workloads", action="store_true", help="add µs/call of every workload to the line")
+    ap.add_argument("--no-per-config", action="store_true", help="leave out the per-workload timings")
+    ap.add_argument("--roofline-calls", type=int, default=1000, help="stage-1 launches timed for the roofline")
+    ap.add_argument("--clock-period-ms", type=float, default=0.5, help="NVML clock sampling period")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fp8-kernel", type=int, default=0, choices=[0, 1],
