@@ -161,6 +161,8 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   p->dev.num_kv_slots = opt.num_kv_slots;
   p->dev.num_ctas = h.num_ctas;
   p->dev.n_reduce = h.n_reduce;
+  p->dev.reduce_max_slots = 0;
+  for (int i = 0; i < h.n_reduce; ++i) p->dev.reduce_max_slots = std::max(p->dev.reduce_max_slots, h.reduce[i].n_slots);
   p->dev.fp8_kernel = opt.fp8_kernel;
   p->dev.dual_issue = mla::dual_issue(opt) ? 1 : 0;
   p->zero_row = base + o_zero;

@@ -104,6 +104,7 @@ struct DevicePlan {
   int64_t num_kv_slots;  // 0 = unchecked
   int num_ctas;
   int n_reduce;
+  int reduce_max_slots;  // most partial slots of any reduce entry (picks the reduce instance)
   int fp8_kernel;        // see PlanOptions
   int dual_issue;        // tcgen05 kernel instance: 1 two MMA issuers, 0 one
 };

@@ -131,6 +131,8 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const float* kv
   p.num_kv_slots = num_kv_slots > 0 ? num_kv_slots : 0;
   p.num_ctas = fp.n_ctas;
   p.n_reduce = fp.n_reduce;
+  p.reduce_max_slots = 0;
+  for (int i = 0; i < fp.n_reduce; ++i) p.reduce_max_slots = std::max(p.reduce_max_slots, fp.reduce[i].n_slots);
   p.dual_issue = 1;
   const DecodeArgs a{q, kv, kv_scale, kv_indptr, kv_indices, out, sm_scale};
   if (launch_stage1(dtype_mode, a, p, base + kZeroOff, stream) != 0) return MLA_ERR_CUDA;

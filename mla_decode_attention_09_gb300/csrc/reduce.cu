@@ -6,11 +6,14 @@
 // out = sum_s 2^{lse_s - L} O_s, rounded to bf16.
 //
 // One CTA of 128 threads per (split sequence, head); each thread owns 4 of the
-// 512 output dims, so every partial row is read once with 16-byte loads. Rows
-// of up to eight slots (the usual case) take one round trip: every thread loads
-// all their LSEs and its parts of all their partial rows at once. Longer rows
-// find the max and the sum of 2^(lse - max) with one slot per lane, and read
-// the partial rows eight slots at a time.
+// 512 output dims, so every partial row is read once with 16-byte loads. A row
+// of up to kBatch slots takes one L2 round trip: lane j of every warp loads the
+// LSE of slot j while every thread loads its 16 bytes of all the partial rows,
+// all in flight at once; the max and the sum of 2^(lse - max) then come from
+// warp shuffles. Longer rows find the max and the sum with one slot per lane,
+// and read the partial rows kBatch slots at a time. Two instances: kBatch = 8
+// (about 64 registers, so a large grid of short rows runs in one wave) and
+// kBatch = 32 (about 160 registers) for plans with longer rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,7 +26,6 @@ namespace mla {
 namespace {
 
 constexpr int kReduceThreads = kVDim / 4;  // 128
-constexpr int kUnroll = 8;
 
 __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
   acc.x = fmaf(w, v.x, acc.x);
@@ -32,6 +34,7 @@ __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
   acc.w = fmaf(w, v.w, acc.w);
 }
 
+template <int kBatch>  // partial rows in flight per thread
 __global__ void __launch_bounds__(kReduceThreads)
     mla_reduce_kernel(const DevicePlan p, __nv_bfloat16* __restrict__ out, int use_pdl) {
   const int e = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
@@ -44,63 +47,51 @@ __global__ void __launch_bounds__(kReduceThreads)
   const int lane = threadIdx.x & 31;
   const int n = r.n_slots;
   const float* lse = p.part_lse + (int64_t)r.slot_begin * kHeads + h;
-  float m = -INFINITY;
-  if (n > kUnroll) {
-    for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[(int64_t)s * kHeads]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int64_t kSlotStride = (int64_t)kHeads * kVDim;
   const float* po = p.part_o + ((int64_t)r.slot_begin * kHeads + h) * kVDim + 4 * threadIdx.x;
-  if (n <= kUnroll) {
-    float4 v[kUnroll];
-    float ls[kUnroll];
+  auto warp_max = [](float x) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (u < n) {
-        ls[u] = lse[(int64_t)u * kHeads];
-        v[u] = __ldcs(reinterpret_cast<const float4*>(po + u * kSlotStride));
-      } else {
-        ls[u] = -INFINITY;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(~0u, x, o));
+    return x;
+  };
+  auto warp_sum = [](float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(~0u, x, o);
+    return x;
+  };
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n <= kBatch) {
+    const float ls = lane < n ? lse[(int64_t)lane * kHeads] : -INFINITY;
+    float4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      v[u] = u < n ? __ldcs(reinterpret_cast<const float4*>(po + u * kSlotStride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float m = warp_max(ls);  // the same in every warp
+    if (m != -INFINITY) {
+      const float wl = exp2f(ls - m);  // 0 for the lanes past the row's slots
+      const float inv_z = 1.0f / warp_sum(wl);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) fma4(acc, __shfl_sync(~0u, wl, u) * inv_z, v[u]);
     }
-    float mx = -INFINITY;
+  } else {
+    float m = -INFINITY;
+    for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[(int64_t)s * kHeads]);
+    m = warp_max(m);
+    if (m != -INFINITY) {
+      float z = 0.f;
+      for (int s = lane; s < n; s += 32) z += exp2f(lse[(int64_t)s * kHeads] - m);
+      const float inv_z = 1.0f / warp_sum(z);
+      for (int s0 = 0; s0 < n; s0 += kBatch) {
+        // lane j holds the weight of slot s0 + j
+        const int cnt = min(kBatch, n - s0);
+        const float wl = lane < cnt ? exp2f(lse[(int64_t)(s0 + lane) * kHeads] - m) * inv_z : 0.f;
+        float4 v[kBatch];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) mx = fmaxf(mx, ls[u]);
-    if (mx != -INFINITY) {
-      float wt[kUnroll], z = 0.f;
+        for (int u = 0; u < kBatch; ++u)
+          v[u] = u < cnt ? __ldcs(reinterpret_cast<const float4*>(po + (s0 + u) * kSlotStride))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        wt[u] = exp2f(ls[u] - mx);  // 0 for the unused slots
-        z += wt[u];
-      }
-      const float inv_z = 1.0f / z;
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) fma4(acc, wt[u] * inv_z, v[u]);
-    }
-  } else if (m != -INFINITY) {
-    float z = 0.f;
-    for (int s = lane; s < n; s += 32) z += exp2f(lse[(int64_t)s * kHeads] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(~0u, z, o);
-    const float inv_z = 1.0f / z;
-    for (int s0 = 0; s0 < n; s0 += 32) {
-      // lane j holds the weight of slot s0 + j
-      const int cnt = min(32, n - s0);
-      const float wl = lane < cnt ? exp2f(lse[(int64_t)(s0 + lane) * kHeads] - m) * inv_z : 0.f;
-      int j = 0;
-      for (; j + kUnroll <= cnt; j += kUnroll) {
-        float4 v[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(po + (s0 + j + u) * kSlotStride));
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) fma4(acc, __shfl_sync(~0u, wl, j + u), v[u]);
-      }
-      for (; j < cnt; ++j) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(po + (s0 + j) * kSlotStride));
-        fma4(acc, __shfl_sync(~0u, wl, j), v);
+        for (int u = 0; u < kBatch; ++u) fma4(acc, __shfl_sync(~0u, wl, u), v[u]);
       }
     }
   }
@@ -124,8 +115,9 @@ int launch_reduce(void* out, const DevicePlan& p, void* stream, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t err =
-      cudaLaunchKernelEx(&cfg, mla_reduce_kernel, p, static_cast<__nv_bfloat16*>(out), pdl ? 1 : 0);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  const cudaError_t err = p.reduce_max_slots > 8 ? cudaLaunchKernelEx(&cfg, mla_reduce_kernel<32>, p, o, pdl ? 1 : 0)
+                                                 : cudaLaunchKernelEx(&cfg, mla_reduce_kernel<8>, p, o, pdl ? 1 : 0);
   return (int)err;
 }
 
