@@ -823,7 +823,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             if (__all_sync(~0u, wait_u(bar(kBPEmpty + (pt & 1)), (pt >> 1) & 1, abort_flag))) {
               umma::fence_after_sync();
               const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
-#pragma unroll
+              // kept as a loop (rare path; see the epilogue's note on code layout)
+#pragma unroll 1
               for (int c16 = 0; c16 < 8; ++c16) {  // 4 blocks x (hi, lo)
                 float o[16];
                 umma::tmem_ld16(ob + 16u * c16, o);
@@ -895,7 +896,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       }
       umma::fence_after_sync();
       const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
-#pragma unroll
+      // Unrolled in the paged instance, a loop in the row instance. This kernel's speed
+      // moves by several µs with the layout of code that runs once per item or less
+      // (measured on one box: the row instance 55.5 µs with both this loop and the
+      // rescale above kept as loops, 56.0 with both unrolled; the paged instance on
+      // shuffled pages of 64, 59.9 µs with this one unrolled, 67.9 with it a loop).
+#pragma unroll(kPaged ? 4 : 1)
       for (int blk = 0; blk < 4; ++blk) {
         float o[16], o_lo[16];
         umma::tmem_ld16(ob + 32u * blk, o);
