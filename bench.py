@@ -261,6 +261,14 @@ def copies_for(bytes_per_copy: int, dev) -> int:
     return max(2, -(-3 * l2 // max(bytes_per_copy, 1)))
 
 
+def gpu_lead(cycles: int = 20_000_000):
+    """Queue ~10 ms of GPU spinning ahead of a timed region's start event: the host
+    then enqueues the region's launches while the GPU is still busy, so a host-side
+    delay (a slow launch call, a driver lock held by the clock sampler) does not
+    fall between the start event and the region's first kernel."""
+    torch.cuda._sleep(cycles)
+
+
 class GraphTimer:
     """K calls of `call(k)` (k = call index) captured in CUDA graphs of `chunk`
     calls each and replayed; CUDA events between replays on the replay stream."""
@@ -291,6 +299,7 @@ class GraphTimer:
         """Returns (total ms, median µs per call over the full replays)."""
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(self.reps + 1)]
         e1 = torch.cuda.Event(enable_timing=True)
+        gpu_lead()
         marks[0].record()
         for k in range(self.reps):
             self.main.replay()
@@ -558,6 +567,7 @@ def bench_e2e(mla, args, w, devs, scales, outs, plan, ws, dev, step_bytes):
     barrier(ws)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    gpu_lead()
     t0.record()
     for _ in range(e2e_steps):
         e2e_step()
