@@ -155,6 +155,15 @@ int mla_plan_release(mla_plan* plan);
 /* Fill *info with the plan's shape. */
 int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info);
 
+/* The same release under the name the split-KV workspace is often given a
+   destroy call by: drops one reference; the last one frees the plan's device
+   memory. Returns MLA_OK or MLA_ERR_ARG (NULL or unknown plan). */
+int mla_plan_destroy(mla_plan* plan);
+
+/* Device bytes the plan owns (work list, reduce map, fp32 partials, error
+   word; mla_plan_info.workspace_bytes). 0 for a NULL plan. */
+size_t mla_plan_workspace_bytes(const mla_plan* plan);
+
 /*
  * mla_decode — one decode call: stage 1 (+ reduce when any sequence is split).
  *   q          device bf16 [B,16,576], row-major, 16-byte aligned.

@@ -39,7 +39,8 @@ STATUS = {
 
 # Every symbol include/mla_decode.h declares.
 EXPORTS = (
-    "mla_decode_plan", "mla_decode_plan_ex", "mla_plan_release", "mla_plan_get_info", "mla_decode",
+    "mla_decode_plan", "mla_decode_plan_ex", "mla_plan_release", "mla_plan_get_info", "mla_plan_destroy",
+    "mla_plan_workspace_bytes", "mla_decode",
     "mla_decode_stage1", "mla_decode_reduce", "mla_plan_check_error", "mla_strerror", "mla_version",
     "mla_plan_compute_host", "mla_decode_noalloc", "mla_decode_plan_paged", "mla_decode_paged",
     "mla_plan_compute_host_paged", "mla_decode_plan_multi", "mla_decode_multi", "mla_plan_compute_host_multi",
@@ -88,6 +89,9 @@ def load_library(path: str | None = None):
         lib.mla_decode_plan_ex.argtypes = [I, V, I, ctypes.POINTER(PlanOptions), ctypes.POINTER(V)]
         lib.mla_plan_release.argtypes = [V]
         lib.mla_plan_get_info.argtypes = [V, ctypes.POINTER(PlanInfo)]
+        lib.mla_plan_destroy.argtypes = [V]
+        lib.mla_plan_workspace_bytes.argtypes = [V]
+        lib.mla_plan_workspace_bytes.restype = ctypes.c_size_t
         dec = [V, V, V, V, V, V, F, I, V, V]
         lib.mla_decode.argtypes = dec
         lib.mla_decode_stage1.argtypes = dec
@@ -107,7 +111,7 @@ def load_library(path: str | None = None):
         lib.mla_plan_compute_host_multi.argtypes = [I, V, V, V, I, I, I, ctypes.POINTER(PlanOptions), V, V, I, V, I,
                                                     V, I]
         for name in EXPORTS:
-            if name not in ("mla_strerror",):
+            if name not in ("mla_strerror", "mla_plan_workspace_bytes"):
                 getattr(lib, name).restype = I
         if path is None:
             _lib = lib

@@ -281,6 +281,10 @@ int mla_plan_release(mla_plan* plan) {
   return MLA_ERR_ARG;
 }
 
+int mla_plan_destroy(mla_plan* plan) { return mla_plan_release(plan); }
+
+size_t mla_plan_workspace_bytes(const mla_plan* plan) { return plan ? plan->block_bytes : 0; }
+
 int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   if (!plan || !info) return MLA_ERR_ARG;
   info->batch = plan->batch;

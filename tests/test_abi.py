@@ -51,6 +51,8 @@ def test_null_arguments_are_rejected_without_a_gpu(lib):
     assert lib.mla_decode_plan(1, None, 0, None) == -1
     assert lib.mla_plan_release(None) == -1
     assert lib.mla_plan_get_info(None, None) == -1
+    assert lib.mla_plan_destroy(None) == -1
+    assert lib.mla_plan_workspace_bytes(None) == 0
     assert lib.mla_decode_reduce(None, None, None) == -1
     assert lib.mla_plan_check_error(None, None) == -1
     args = [None] * 6 + [ctypes.c_float(0.1), 0, None, None]
