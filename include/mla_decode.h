@@ -89,9 +89,10 @@ typedef struct mla_plan_options {
   int64_t num_kv_slots;   /* rows in the KV pool; kv_indices are checked against it in the
                              kernel (out-of-range rows are skipped and MLA_ERR_INDEX recorded).
                              0 = unchecked (the plain mla_decode_plan) */
-  int min_rows_per_split; /* smallest KV chunk the planner cuts (default 128, one tile) */
+  int min_rows_per_split; /* smallest KV chunk the planner cuts (default 64) */
   int granularity;        /* work is balanced in units of this many rows, and chunk boundaries fall on
-                             multiples of it from the sequence start (default 128, the fp8 kernel's tile) */
+                             multiples of it from the sequence start (default 64: the warp-level kernels'
+                             tile, half the tensor-memory kernel's) */
   int ctas_per_sm;        /* persistent CTAs per SM (default 1) */
   int fp8_kernel;         /* fp8 stage-1 kernel: 0 = 5th-generation tensor cores (tcgen05 + TMA, default),
                              1 = warp-level mma.sync (kept for comparison) */

@@ -32,8 +32,8 @@ static_assert(kEnd <= kScratchBytes, "scratch layout exceeds the array");
 static_assert(kZeroOff % 256 == 0 && kLseOff % 256 == 0 && kIndptrOff % 256 == 0, "alignment");
 
 // Work list in fixed-capacity arrays (no heap): the same split as the
-// regular planner with its default options (128-row granules balanced across
-// CTAs, chunks of at least 128 rows, one CTA per SM).
+// regular planner with its default options (64-row granules balanced across
+// CTAs, chunks of at least 64 rows, one CTA per SM), without its cost per item.
 struct FixedPlan {
   WorkItem items[kMaxItems];
   int32_t indptr[kMaxCtas + 1];
@@ -44,7 +44,7 @@ struct FixedPlan {
 
 // Returns MLA_OK, MLA_ERR_INDPTR, or MLA_ERR_NOALLOC_LIMIT when a fixed capacity is exceeded.
 inline int plan_fixed(int batch, const int32_t* ip, int num_sms, FixedPlan* fp) {
-  constexpr int64_t G = 128, kMinRows = 128;
+  constexpr int64_t G = 64, kMinRows = 64;
   if (ip[0] != 0) return MLA_ERR_INDPTR;
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) {

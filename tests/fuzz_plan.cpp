@@ -135,16 +135,16 @@ int main(int argc, char** argv) {
     const char* e = check_rows(B, ip.data(), fp->items, fp->n_items, fp->indptr, fp->n_ctas, fp->reduce,
                                fp->n_reduce, fp->n_slots);
     if (e) { printf("fixed plan: %s (iter %d, B %d, sms %d)\n", e, iter, B, num_sms); return 1; }
-    // balance: no CTA holds more than the even share of 128-row granules, rounded up,
-    // and at least one 128-row granule when there are rows
+    // balance: no CTA holds more than the even share of 64-row granules, rounded up,
+    // and at least one granule when there are rows
     int64_t granules = 0;
-    for (int b = 0; b < B; ++b) granules += (ip[b + 1] - ip[b] + 127) / 128;
+    for (int b = 0; b < B; ++b) granules += (ip[b + 1] - ip[b] + 63) / 64;
     const int64_t share = std::max<int64_t>(1, (granules + std::min(num_sms, noalloc::kMaxCtas) - 1) /
                                                    std::min(num_sms, noalloc::kMaxCtas));
     for (int c = 0; c < fp->n_ctas; ++c) {
       int64_t g = 0;
       for (int i = fp->indptr[c]; i < fp->indptr[c + 1]; ++i)
-        g += (fp->items[i].t_end - fp->items[i].t_begin + 127) / 128;
+        g += (fp->items[i].t_end - fp->items[i].t_begin + 63) / 64;
       if (g > share + 1) { printf("fixed plan: cta %d holds %lld granules, share %lld\n", c, (long long)g, (long long)share); return 1; }
     }
   }

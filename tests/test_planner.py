@@ -25,8 +25,8 @@ def _check_plan(lengths, num_sms, **opts):
     ip[1:] = np.cumsum(lengths)
     r = mla.plan_compute_host(ip, num_sms, **opts)
     items, wip, red = r["items"], r["work_indptr"], r["reduce"]
-    G = opts.get("granularity", 128)
-    min_split = opts.get("min_rows_per_split", 128)
+    G = opts.get("granularity", 64)
+    min_split = opts.get("min_rows_per_split", 64)
     cpsm = opts.get("ctas_per_sm", 1)
     total = int(ip[-1])
     # CTA ranges: CSR over the item list, at most num_sms * ctas_per_sm CTAs
@@ -122,8 +122,11 @@ def test_plan_headline_shapes():
     r = _check_plan([8192] * 64, 152)
     assert 150 <= r["num_ctas"] <= 152
     assert 64 * 2 <= r["num_slots"] <= 64 * 4
-    # B=4 x 1024 bf16: small problem, one 128-row tile per CTA (the minimum chunk)
+    # B=4 x 1024 bf16: small problem, one 64-row granule per CTA (the default minimum chunk)
     r = _check_plan([1024] * 4, 152)
+    assert r["num_ctas"] == 64
+    # with 128-row granules (the tensor-memory kernel's tile), one tile per CTA
+    r = _check_plan([1024] * 4, 152, granularity=128, min_rows_per_split=128)
     assert r["num_ctas"] == 32
     # B=64 x 8192, 4096 tiles. Without item costs every CTA gets 27 tiles at most. With the
     # default cost of two tiles per item, CTAs that hold two sequence pieces get fewer tiles
@@ -136,9 +139,10 @@ def test_plan_headline_shapes():
             n.append(len(its))
         return np.array(t), np.array(n)
     ip = np.arange(65, dtype=np.int32) * 8192
-    t, n = tiles_items(mla.plan_compute_host(ip, 152, item_cost_rows=-1))
+    g128 = dict(granularity=128, min_rows_per_split=128)
+    t, n = tiles_items(mla.plan_compute_host(ip, 152, item_cost_rows=-1, **g128))
     assert t.sum() == 4096 and t.max() == 27 and (t + 2 * n).max() == 31
-    t, n = tiles_items(mla.plan_compute_host(ip, 152))
+    t, n = tiles_items(mla.plan_compute_host(ip, 152, **g128))
     assert t.sum() == 4096 and (t + 2 * n).max() == 30 and len(t) >= 150
     assert t[n == 2].max() < t[n == 1].max()
 
@@ -265,7 +269,8 @@ def test_multi_plan_balances_weighted_granules():
     ip[1:] = np.cumsum(lengths)
     qo = np.zeros(len(q_lens) + 1, dtype=np.int32)
     qo[1:] = np.cumsum(q_lens)
-    r = mla.plan_compute_host_multi(qo, ip, 20, causal=False, item_cost_rows=-1)
+    r = mla.plan_compute_host_multi(qo, ip, 20, causal=False, item_cost_rows=-1, granularity=128,
+                                    min_rows_per_split=128)
     items, wip = r["items"], r["work_indptr"]
     w = [sum(-(-int(items[i, 2] - items[i, 1]) // 128) for i in range(wip[c], wip[c + 1]))
          for c in range(r["num_ctas"])]
