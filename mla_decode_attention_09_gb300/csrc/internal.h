@@ -182,5 +182,7 @@ __device__ __forceinline__ int64_t token_row(const DecodeArgs& a, int32_t e, int
 int launch_stage1(int dtype_mode, const DecodeArgs& a, const DevicePlan& p, const void* zero_row, void* stream);
 int launch_reduce(void* out, const DevicePlan& p, void* stream, bool pdl);
 int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* stream);
+// a16w8 on the tensor cores: the bf16 query as two e4m3 terms (stage1_umma_a16.cu).
+int launch_stage1_a16w8_umma(const DecodeArgs& a, const DevicePlan& p, void* stream);
 
 }  // namespace mla

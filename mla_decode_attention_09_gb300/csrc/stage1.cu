@@ -611,7 +611,9 @@ int launch_stage1(int dtype_mode, const DecodeArgs& a, const DevicePlan& p, cons
   const uint8_t* z = static_cast<const uint8_t*>(zero_row);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype_mode == MLA_MODE_BF16) return launch_stage1_t<MLA_MODE_BF16>(a, p, z, s);
-  if (dtype_mode == MLA_MODE_A16W8) return launch_stage1_t<MLA_MODE_A16W8>(a, p, z, s);
+  // fp8 and a16w8 run on the tensor-memory kernel unless the plan asks for the warp-level one
+  if (dtype_mode == MLA_MODE_A16W8)
+    return p.fp8_kernel == 1 ? launch_stage1_t<MLA_MODE_A16W8>(a, p, z, s) : launch_stage1_a16w8_umma(a, p, stream);
   if (p.fp8_kernel == 1) return launch_stage1_t<MLA_MODE_FP8>(a, p, z, s);
   return launch_stage1_fp8_umma(a, p, stream);
 }
