@@ -15,9 +15,13 @@
 // the lazy running max, the epilogue and the bounded waits.
 //
 // What differs from the fp8 kernel:
-// - The staged query is 18 KB. To fit, this kernel keeps one rope slot and one
-//   P buffer. A tile's rope part is then loaded once the previous tile's scores
-//   are done, and its scores wait for the previous tile's softmax.
+// - The staged query is 18 KB. To fit, a tile's P lives in that tile's rope
+//   slot: the rope bytes are dead once the tile's scores are done, and the slot
+//   takes the next rope part once the tile's P.V is done. The two rope slots
+//   are then the two P buffers, and no shared memory is spent on P.
+// - The shared memory then holds 68 bytes less than the slack the fp8 kernel
+//   keeps for rounding the dynamic base up to 1024 bytes; this kernel needs the
+//   base aligned already, checks it, and stops with MLA_ERR_DEVICE otherwise.
 // - The softmax warps stage every item's query, not only the first: they need
 //   its scale. They load the next item's query during the current item's last
 //   tile and stage it once that tile's scores are done (the buffer is free).
@@ -77,10 +81,10 @@ constexpr uint32_t kLayoutSw64 = 4;
 enum : int {
   kBFull = 0,     // [3] tile data landed (TMA tx, and every loader lane's cp.async arrival)
   kBLEmpty = 3,   // [3] latent slot free (P.V done)
-  kBREmpty = 6,   // rope slot free (scores done); one slot here, [1] unused
+  kBREmpty = 6,   // [2] rope slot free (the tile's P.V done: the slot held its P)
   kBSFull = 8,    // [2] S^T ready
-  kBPFull = 10,   // P^T written (128 arrivals); one buffer here, [1] unused
-  kBPEmpty = 12,  // P^T consumed (P.V done); one buffer here, [1] unused
+  kBPFull = 10,   // [2] P^T written into the rope slot (128 arrivals)
+  kBPEmpty = 12,  // [2] P^T consumed (P.V done)
   kBQFull = 14,   // query staged (32 arrivals)
   kBQEmpty = 15,  // query consumed (last scores of the item done)
   kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals)
@@ -88,9 +92,9 @@ enum : int {
   kNumBars = 19
 };
 
-// The query as two e4m3 terms of 16 heads each: a 32-row B matrix. One rope
-// slot and one P buffer make room for it.
-constexpr int kRopeStages = 1;
+// The query as two e4m3 terms of 16 heads each: a 32-row B matrix. Each tile's
+// P is written into its rope slot to make room for it.
+constexpr int kRopeStages = 2;
 constexpr int kNQ = 32;                           // B rows of the score MMA
 constexpr int kQKBlk = kNQ * 128;                 // one 128-dim K-block of the staged query (4 KB)
 constexpr int kQLat = 4 * kQKBlk;                 // latent part, 128-byte swizzle (16 KB)
@@ -99,9 +103,8 @@ constexpr uint32_t kIdescQK = umma::idesc_e4m3(128, kNQ, 0, 0);
 
 struct SU {
   static constexpr int kLat = 0;                               // 3 x 64 KB
-  static constexpr int kRope = kLat + kLatStages * kLatStage;  // 1 x 8 KB
-  static constexpr int kP = kRope + kRopeStages * kRopeStage;  // 1 x 4 KB
-  static constexpr int kQ = kP + kPBuf;                        // 18 KB
+  static constexpr int kRope = kLat + kLatStages * kLatStage;  // 2 x 8 KB: rope part, then the tile's P
+  static constexpr int kQ = kRope + kRopeStages * kRopeStage;  // 18 KB
   static constexpr int kRed = kQ + kQBytes;                    // [2][16 heads][4 warps] fp32 tile max
   static constexpr int kLsum = kRed + 2 * 64 * 4;              // [16 heads][4 warps] fp32 row sums
   static constexpr int kBar = kLsum + 64 * 4;
@@ -110,11 +113,11 @@ struct SU {
   static constexpr int kRowCopy = kAbort + 4;                  // [3] latent slot holds a row-copied tile
   static constexpr int kQMax = kRowCopy + 3 * 4;               // [4 warps] query max exchange
   static constexpr int kBytes = kQMax + 4 * 4;
-  static constexpr int kAlloc = kBytes + 1024;                 // the base is rounded up to 1024 inside the kernel
+  static constexpr int kAlloc = kBytes;                        // the dynamic base must be 1024-aligned
 };
 static_assert(SU::kAlloc <= 232448, "a16w8 tcgen05 stage-1 shared memory");
-static_assert(SU::kQ % 1024 == 0 && SU::kRope % 1024 == 0 && SU::kP % 16 == 0 && SU::kBar % 8 == 0,
-              "operand alignment");
+static_assert(SU::kQ % 1024 == 0 && SU::kRope % 1024 == 0 && SU::kBar % 8 == 0, "operand alignment");
+static_assert(kPBuf <= kRopeStage, "a tile's P fits in its rope slot");
 
 __device__ __forceinline__ void record_error_u(int* err, int code) { atomicCAS(err, 0, code); }
 
@@ -282,11 +285,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   constexpr int kLoaders = 2;  // tiles copied row by row are split between warps 4 and 7
 
   // 1024-aligned base for the swizzle atoms
-  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
-  const uint32_t base = (raw_addr + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw_addr);
+  // The swizzle atoms need 1024-aligned buffers and the allocation has no room to
+  // round the base up: without an aligned base the CTA touches nothing and stops.
+  const uint32_t base = ptx::smem_addr(smem_raw);
+  if (base & 1023u) {
+    if (threadIdx.x == 0) record_error_u(p.err, MLA_ERR_DEVICE);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t lat_addr = base + SU::kLat, rope_addr = base + SU::kRope, q_addr = base + SU::kQ;
-  const uint32_t p_addr = base + SU::kP;
   float* red = reinterpret_cast<float*>(smem + SU::kRed);
   float* lsum = reinterpret_cast<float*>(smem + SU::kLsum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SU::kAbort);
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 
   // MMA issue of one tile (one thread): scores, and P.V
   auto issue_qk = [&](const TCur& c, int i) {
-    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr;  // one rope slot
+    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
     const uint32_t d = tmem + kColS + (uint32_t)kNQ * (uint32_t)(i & 1);
     umma::fence_after_sync();
     // row-copied tile: order the cp.async (generic proxy) writes before the tensor core reads them
@@ -360,13 +367,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     for (int st = 0; st < 2; ++st)
       umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
                        umma::smem_desc(q_addr + kQLat + st * 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
-    umma::commit(bar(kBSFull + (i & 1)));
-    umma::commit(bar(kBREmpty));
+    umma::commit(bar(kBSFull + (i & 1)));  // the rope slot frees only after the tile's P.V (it takes P)
     if (c.t0 + kRowsU >= c.t_end) umma::commit(bar(kBQEmpty));
   };
   auto issue_pv = [&](const TCur& d, int i) {
     const bool first = d.t0 == d.t_begin;
-    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = p_addr;  // one P buffer
+    // P^T of tile i sits in tile i's rope slot
+    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = rope_addr + (i & 1) * kRopeStage;
     const uint32_t ob = tmem + kColO + 128u * (uint32_t)(d.k & 1);
     umma::fence_after_sync();
     // B = [P_hi^T | P_lo^T], MN-major without swizzle: 8-token core matrices 128 B apart
@@ -378,7 +385,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         umma::mma_f8f6f4(ob + 32u * blk, umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128),
                          umma::smem_desc(p0 + j * 512, 128, kPLo, umma::kLayoutNone), kIdescPV,
                          (first && j == 0) ? 0u : 1u);
-    umma::commit(bar(kBPEmpty));
+    umma::commit(bar(kBPEmpty + (i & 1)));
+    umma::commit(bar(kBREmpty + (i & 1)));
     umma::commit(bar(kBLEmpty + i % kLatStages));
   };
 
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     while (!c.done) {
       bool progress = false;
       if (!c.done) {
-        const int ls = i % kLatStages;
+        const int ls = i % kLatStages, rs = i & 1;
         const int nv = c.t_end - c.t0;
         if (!decided) {
           // Box loads when the valid rows are consecutive. A tail tile may then
@@ -479,13 +487,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         bool ready;
         if (main_loader) {  // polls: it also stages queries
           ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
-          // the one rope slot is free once the previous tile's scores are done
-          ready = ready && (i < 1 || ptx::mbar_test_wait(bar(kBREmpty), (i - 1) & 1));
+          // the rope slot is free once P.V of the tile two before is done
+          ready = ready && (i < 2 || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
           ready = __shfl_sync(~0u, ready, 0);
         } else {  // the extra loaders have nothing else to do: a bounded blocking wait
           const bool w_ok =
               (i < kLatStages || wait_u(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1, abort_flag)) &&
-              (i < 1 || wait_u(bar(kBREmpty), (i - 1) & 1, abort_flag));
+              (i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag));
           if (!__all_sync(~0u, w_ok)) {
             ok = false;
             break;
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
         if (ready) {
           const uint32_t fb = bar(kBFull + ls);
-          const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr;
+          const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
           if (main_loader && lane == 0) row_copy[ls] = (cont || runs) ? 0 : 1;  // published by the arrivals below
           if (runs) {
             if (main_loader) {
@@ -578,9 +586,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // ------------------------------------------------ score MMAs (one thread)
     // Scores of tile j need the item's query (first tile), the tile's data, and
     // the S buffer: the softmax of tile j - 2 has read it (its P is written).
-    // With one P buffer, whose phases are every tile's, a wait for tile j - 2's
-    // phase could alias a phase two later: the issuer waits for tile j - 1's
-    // softmax instead (the one rope slot holds tile j back until then anyway).
     if (lane == 0) {
       bool ok = true;
       TCur c;
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       while (!c.done) {
         ok = (c.t0 != c.t_begin || wait_u(bar(kBQFull), c.k & 1, abort_flag)) &&
              wait_u(bar(kBFull + nq % kLatStages), (nq / kLatStages) & 1, abort_flag) &&
-             (nq < 1 || wait_u(bar(kBPFull), (nq - 1) & 1, abort_flag));
+             (nq < 2 || wait_u(bar(kBPFull + (nq & 1)), ((nq - 2) >> 1) & 1, abort_flag));
         if (!ok) break;
         issue_qk(c, nq);
         ++nq;
@@ -613,7 +618,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       while (!d.done) {
         const bool first = d.t0 == d.t_begin;
         ok = (!first || d.k < 2 || wait_u(bar(kBOEmpty + (d.k & 1)), ((d.k >> 1) - 1) & 1, abort_flag)) &&
-             wait_u(bar(kBPFull), npv & 1, abort_flag);
+             wait_u(bar(kBPFull + (npv & 1)), (npv >> 1) & 1, abort_flag);
         if (!ok) break;
         issue_pv(d, npv);
         ++npv;
@@ -770,7 +775,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           }
           if (!first) {  // move the reference up: rescale O once P.V of the previous tile has landed
             const int pt = i - 1;
-            if (__all_sync(~0u, wait_u(bar(kBPEmpty), pt & 1, abort_flag))) {
+            if (__all_sync(~0u, wait_u(bar(kBPEmpty + (pt & 1)), (pt >> 1) & 1, abort_flag))) {
               umma::fence_after_sync();
               const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
               // kept as a loop (rare path; see the epilogue's note on code layout)
@@ -816,16 +821,17 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(vrow + cb * kBlk + ch * 16) = make_uint4(0, 0, 0, 0);
         }
-        // one P buffer: P.V of the previous tile has read it
-        if (ok && i >= 1) ok = wait_u(bar(kBPEmpty), (i - 1) & 1, abort_flag);
+        // P goes into this tile's rope slot: its scores are done (S was full), and
+        // the P.V two tiles before, which used the slot last, has landed
+        if (ok && i >= 2) ok = wait_u(bar(kBPEmpty + (i & 1)), ((i >> 1) - 1) & 1, abort_flag);
         if (ok) {
-          uint8_t* pb = smem + SU::kP + row * 16;
+          uint8_t* pb = smem + SU::kRope + (i & 1) * kRopeStage + row * 16;
           *reinterpret_cast<uint4*>(pb) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(pb + kPLo) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
         }
         umma::fence_proxy_async_smem();
         umma::fence_before_sync();
-        umma::mbar_arrive(bar(kBPFull));
+        umma::mbar_arrive(bar(kBPFull + (i & 1)));
         // this item's last scores are done (S was full), so the query buffer is
         // free: stage the next item's query now (its scale applies from that item on)
         if (stage_next) e_cur = stage_split(nraw);
@@ -836,7 +842,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       const float lh = xreduce16<false>(l, lane);
       if (!(lane & 1)) lsum[(lane >> 1) * 4 + warp] = lh;
       const int tl = i - 1;
-      bool ok = wait_u(bar(kBPEmpty), tl & 1, abort_flag);
+      bool ok = wait_u(bar(kBPEmpty + (tl & 1)), (tl >> 1) & 1, abort_flag);
       if (ptx::named_bar_or(1, 128, !ok)) {
         aborted = true;
         break;
