@@ -196,6 +196,9 @@ STAGE1_KERNELS = {
     # kernel name -> (profile file stem, sources whose bytes identify the compiled kernel)
     "mla_stage1_fp8_umma_kernel": ("stage1_umma", ("stage1_umma.cu", "umma.cuh", "ptx.cuh", "internal.h")),
     "mla_stage1_kernel": ("stage1_mma", ("stage1.cu", "ptx.cuh", "internal.h")),
+    "mla_stage1_a16w8_umma_kernel": ("stage1_umma_a16", ("stage1_umma_a16.cu", "umma.cuh", "ptx.cuh", "internal.h")),
+    "mla_stage1_fp8_pairs_umma_kernel": ("stage1_umma_pairs",
+                                         ("stage1_umma_pairs.cu", "umma.cuh", "ptx.cuh", "internal.h")),
 }
 
 
@@ -372,7 +375,7 @@ def bench_ours(args):
             qh, qo = mi.make_query_tokens([q_len] * w.batch, seed=w.seed + 50 + replica_seed_offset(rank, k))
             queries.append((qh.to(dev), qo.to(dev)))
         plan = mla.plan_multi(queries[0][1].cpu(), devs[0].kv_indptr.cpu(), causal=True, page_size=page_size,
-                              kv_last_page_len_host=last_host, **opts)
+                              kv_last_page_len_host=last_host, token_pairs=args.token_pairs, **opts)
     elif kind == "pages":
         plan = mla.plan_paged(devs[0].kv_indptr.cpu(), last_host, page_size, **opts)
     else:
@@ -430,8 +433,12 @@ def bench_ours(args):
         kern_us = ms_per_step * 1e3
     sampler.mark(None)
     achieved = step_bytes / (kern_us * 1e-6) / 1e9
-    kernel = ("mla_stage1_fp8_umma_kernel" if (w.mode == mi.MODE_FP8 and args.fp8_kernel == 0)
-              else "mla_stage1_kernel")
+    if args.fp8_kernel == 1 or w.mode == mi.MODE_BF16:
+        kernel = "mla_stage1_kernel"
+    elif w.mode == mi.MODE_A16W8:
+        kernel = "mla_stage1_a16w8_umma_kernel"
+    else:
+        kernel = "mla_stage1_fp8_pairs_umma_kernel" if plan.token_pairs else "mla_stage1_fp8_umma_kernel"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": ncu_traffic(kernel, args.workload) if default_layout else None,
@@ -478,7 +485,8 @@ def bench_ours(args):
         "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
                    "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": page_size,
                    "kv_order": "shuffled" if shuffled else ("workload" if kind == "rows" else "in order"),
-                   "q_len": q_len, "causal": q_len > 1, "bytes_per_call": step_bytes,
+                   "q_len": q_len, "causal": q_len > 1, "token_pairs": bool(plan.token_pairs),
+                   "bytes_per_call": step_bytes,
                    "l2": (f"{n_copies} input copies rotate call after call "
                           + ("(each larger than L2)" if n_copies == 2 and step_bytes > l2_bytes(dev)
                              else "(together three times L2)")),
@@ -643,6 +651,8 @@ def main():
     ap.add_argument("--layout", default="rows",
                     help="KV layout of the workload: rows (its own order), rows:shuffled, pages:N, pages:N:shuffled")
     ap.add_argument("--q-len", type=int, default=1, help="query tokens per sequence (causal)")
+    ap.add_argument("--token-pairs", type=int, default=0, choices=[0, 1],
+                    help="several query tokens, fp8: plan tokens in pairs, one pass over the rows per pair")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

@@ -110,6 +110,14 @@ typedef struct mla_plan_options {
                              token and give each range Q CTAs, one per token, which read the same rows
                              at the same time (from HBM once, from L2 for the others). 0 = default (on);
                              negative = off: each range's tokens run back to back in one CTA. */
+  int token_pairs;        /* several query tokens, fp8 only: when every sequence with KV rows has the same
+                             even number Q of query tokens, take tokens 2v and 2v+1 of a sequence in one
+                             pass over their rows (both queries in one 32-column score MMA), which reads
+                             each KV tile once for two tokens. token_parallel then applies to the Q/2
+                             pairs. > 0 = on; 0 = default (off). A plan made with pairs serves only
+                             mla_decode_multi with dtype_mode MLA_MODE_FP8 on the tensor-core kernel
+                             (fp8_kernel 0); other modes return MLA_ERR_ARG. Without an even, equal Q
+                             the plan is the ordinary one. */
 } mla_plan_options;
 
 /* Read-only description of a plan. */
@@ -123,6 +131,7 @@ typedef struct mla_plan_info {
   int64_t total_rows;     /* sum of the sequence lengths */
   int64_t max_rows_per_cta;
   size_t workspace_bytes; /* device bytes the plan owns */
+  int token_pairs;        /* 1: the work items are token pairs (option token_pairs took effect) */
 } mla_plan_info;
 
 /*
@@ -372,9 +381,16 @@ int mla_decode_plan_multi(int batch, const int32_t* qo_indptr_host, const int32_
 int mla_decode_multi(const void* q, const void* kv, const float* kv_scale, const int32_t* qo_indptr,
                      const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
                      int page_size, void* out, float sm_scale, int dtype_mode, mla_plan* workspace, void* stream);
-/* mla_plan_compute_host for multi-token plans: items as int32 [items_cap][7] =
+/* mla_plan_compute_host for multi-token plans: items as int32 [items_cap][8] =
    (sequence, first token, end token, partial slot or -1, sequence length,
-   query row, query token within the sequence). */
+   query row, query token within the sequence, pair field), and the reduce map
+   as int32 [reduce_cap][4] = (query row, first slot, slots, slot stride).
+   The pair field is 0 in ordinary plans. In token-pair plans an item with pair
+   field >= 0 covers query rows r and r + 1 (tokens j and j + 1): row r sees
+   tokens [first, pair field), row r + 1 tokens [first, end), and their partial
+   slots are slot and slot + 1; -1 marks an item of one query row (a sequence
+   without KV rows). The slot stride is 0 (consecutive slots) or 2 (a row of a
+   token pair). */
 int mla_plan_compute_host_multi(int batch, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                                 const int32_t* kv_last_page_len_host, int page_size, int causal, int num_sms,
                                 const mla_plan_options* options, int32_t* counts, int32_t* items, int items_cap,

@@ -57,14 +57,14 @@ class PlanOptions(ctypes.Structure):
     _fields_ = [("num_kv_slots", ctypes.c_int64), ("min_rows_per_split", ctypes.c_int),
                 ("granularity", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("fp8_kernel", ctypes.c_int),
                 ("fp8_issuers", ctypes.c_int), ("item_cost_rows", ctypes.c_int),
-                ("token_parallel", ctypes.c_int)]
+                ("token_parallel", ctypes.c_int), ("token_pairs", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("num_ctas", ctypes.c_int), ("num_work_items", ctypes.c_int),
                 ("num_partial_slots", ctypes.c_int), ("num_split_seqs", ctypes.c_int), ("device", ctypes.c_int),
                 ("total_rows", ctypes.c_int64), ("max_rows_per_cta", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("token_pairs", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -131,9 +131,10 @@ def _check(status: int, what: str):
 
 
 def _opts(num_kv_slots=0, min_rows_per_split=0, granularity=0, ctas_per_sm=0, fp8_kernel=0,
-          fp8_issuers=0, item_cost_rows=0, token_parallel=0) -> PlanOptions:
+          fp8_issuers=0, item_cost_rows=0, token_parallel=0, token_pairs=0) -> PlanOptions:
     return PlanOptions(int(num_kv_slots), int(min_rows_per_split), int(granularity), int(ctas_per_sm),
-                       int(fp8_kernel), int(fp8_issuers), int(item_cost_rows), int(token_parallel))
+                       int(fp8_kernel), int(fp8_issuers), int(item_cost_rows), int(token_parallel),
+                       int(token_pairs))
 
 
 def _host_indptr(kv_indptr) -> torch.Tensor:
@@ -184,6 +185,11 @@ class Plan:
     @property
     def handle(self):
         return self._handle
+
+    @property
+    def token_pairs(self) -> bool:
+        """The plan's items are token pairs (served by the fp8 tensor-core pair kernel only)."""
+        return bool(self.info()["token_pairs"])
 
     def info(self) -> dict:
         inf = PlanInfo()
@@ -406,7 +412,8 @@ def plan_compute_host_paged(kv_indptr_host, kv_last_page_len_host, page_size: in
 
 def plan_compute_host_multi(qo_indptr_host, kv_indptr_host, num_sms: int, *, causal: bool = True,
                             page_size: int = 1, kv_last_page_len_host=None, **options) -> dict:
-    """plan_compute_host for multi-token plans; items have 7 fields (..., query row, query token)."""
+    """plan_compute_host for multi-token plans; items have 8 fields (..., query row, query token, pair
+    field) and reduce entries 4 (..., slot stride)."""
     import numpy as np
 
     lib = load_library()
@@ -421,9 +428,9 @@ def plan_compute_host_multi(qo_indptr_host, kv_indptr_host, num_sms: int, *, cau
     _check(lib.mla_plan_compute_host_multi(*args, counts.ctypes.data, None, 0, None, 0, None, 0),
            "mla_plan_compute_host_multi")
     n_items, n_ctas, n_slots, n_reduce = (int(x) for x in counts)
-    items = np.zeros((max(n_items, 1), 7), dtype=np.int32)
+    items = np.zeros((max(n_items, 1), 8), dtype=np.int32)
     wip = np.zeros(n_ctas + 1, dtype=np.int32)
-    red = np.zeros((max(n_reduce, 1), 3), dtype=np.int32)
+    red = np.zeros((max(n_reduce, 1), 4), dtype=np.int32)
     _check(lib.mla_plan_compute_host_multi(*args, counts.ctypes.data, items.ctypes.data, items.shape[0],
                                            wip.ctypes.data, wip.shape[0], red.ctypes.data, red.shape[0]),
            "mla_plan_compute_host_multi")

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmla_decode.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-CUDA_SOURCES = ["stage1.cu", "stage1_umma.cu", "stage1_umma_a16.cu", "reduce.cu", "noalloc.cu"]
+CUDA_SOURCES = ["stage1.cu", "stage1_umma.cu", "stage1_umma_a16.cu", "stage1_umma_pairs.cu", "reduce.cu", "noalloc.cu"]
 CXX_SOURCES = ["plan.cpp", "capi.cpp"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 

@@ -63,7 +63,7 @@ bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, c
          p->opt.min_rows_per_split == o.min_rows_per_split && p->opt.granularity == o.granularity &&
          p->opt.ctas_per_sm == o.ctas_per_sm && p->opt.fp8_kernel == o.fp8_kernel &&
          p->opt.fp8_issuers == o.fp8_issuers && p->opt.item_cost_rows == o.item_cost_rows &&
-         p->opt.token_parallel == o.token_parallel &&
+         p->opt.token_parallel == o.token_parallel && p->opt.token_pairs == o.token_pairs &&
          std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0 &&
          same_array(p->last_page_len, l.last, (size_t)batch) &&
          same_array(p->qo_indptr, l.qo, batch > 0 ? (size_t)batch + 1 : 0);
@@ -165,6 +165,7 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   for (int i = 0; i < h.n_reduce; ++i) p->dev.reduce_max_slots = std::max(p->dev.reduce_max_slots, h.reduce[i].n_slots);
   p->dev.fp8_kernel = opt.fp8_kernel;
   p->dev.dual_issue = mla::dual_issue(opt) ? 1 : 0;
+  p->dev.token_pairs = h.token_pairs ? 1 : 0;
   p->zero_row = base + o_zero;
   p->refcount = 1;
   *out = p;
@@ -180,6 +181,8 @@ int validate_decode(const void* q, const void* kv, const float* kv_scale, const 
   if (l.kind == kMultiKind && plan->batch > 0 && !l.qo) return MLA_ERR_ARG;
   if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8 && dtype_mode != MLA_MODE_A16W8)
     return MLA_ERR_DTYPE;
+  // token-pair items are understood by the fp8 tensor-core pair kernel only
+  if (plan->dev.token_pairs && (dtype_mode != MLA_MODE_FP8 || plan->dev.fp8_kernel != 0)) return MLA_ERR_ARG;
   if (plan->batch > 0) {
     if (!q || !kv || !kv_indptr || !out) return MLA_ERR_ARG;
     if (plan->host.total_rows > 0 && !kv_indices) return MLA_ERR_ARG;
@@ -230,7 +233,9 @@ int plan_common(int batch, const int32_t* kv_indptr_host, const Layout& layout, 
 
 int decode_common(const mla::DecodeArgs& a, int dtype_mode, mla_plan* workspace, void* stream, bool reduce) {
   if (workspace->batch == 0) return MLA_OK;
-  if (mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream) != 0) return MLA_ERR_CUDA;
+  const int rc = workspace->dev.token_pairs ? mla::launch_stage1_fp8_pairs_umma(a, workspace->dev, stream)
+                                            : mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream);
+  if (rc != 0) return MLA_ERR_CUDA;
   // the reduce is launched programmatically dependent: it starts while stage 1
   // drains and waits for its results on the device
   if (reduce && mla::launch_reduce(a.out, workspace->dev, stream, true) != 0) return MLA_ERR_CUDA;
@@ -296,6 +301,7 @@ int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   info->total_rows = plan->host.total_rows;
   info->max_rows_per_cta = plan->host.max_rows_per_cta;
   info->workspace_bytes = plan->block_bytes;
+  info->token_pairs = plan->dev.token_pairs;
   return MLA_OK;
 }
 
@@ -429,8 +435,8 @@ int mla_plan_compute_host(int batch, const int32_t* kv_indptr_host, int num_sms,
 
 int mla_plan_compute_host_multi(int batch, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                                 const int32_t* kv_last_page_len_host, int page_size, int causal, int num_sms,
-                                const mla_plan_options* options, int32_t* counts4, int32_t* items7, int items_cap,
-                                int32_t* work_indptr, int indptr_cap, int32_t* reduce3, int reduce_cap) {
+                                const mla_plan_options* options, int32_t* counts4, int32_t* items8, int items_cap,
+                                int32_t* work_indptr, int indptr_cap, int32_t* reduce4, int reduce_cap) {
   try {
     if (!counts4) return MLA_ERR_ARG;
     mla::HostPlan h;
@@ -438,19 +444,26 @@ int mla_plan_compute_host_multi(int batch, const int32_t* qo_indptr_host, const 
     const int rc = mla::build_host_plan_multi(batch, batch > 0 ? qo_indptr_host : &kZero,
                                               batch > 0 ? kv_indptr_host : &kZero, kv_last_page_len_host, page_size,
                                               causal != 0, num_sms, mla::resolve_options(options), &h);
-    if (rc == MLA_OK && items7 && items_cap >= h.n_items)
+    if (rc == MLA_OK && items8 && items_cap >= h.n_items)
       for (int i = 0; i < h.n_items; ++i) {
-        items7[7 * i + 5] = h.items[i].q_row;
-        items7[7 * i + 6] = h.items[i].q_tok;
+        items8[8 * i + 5] = h.items[i].q_row;
+        items8[8 * i + 6] = h.items[i].q_tok;
+        items8[8 * i + 7] = h.items[i].pad;
       }
-    // the first five fields of every item, at a stride of seven
-    std::vector<int32_t> five(items7 && rc == MLA_OK && items_cap >= h.n_items ? (size_t)h.n_items * 5 : 0);
-    const int n_items = rc == MLA_OK ? h.n_items : 0;
+    if (rc == MLA_OK && reduce4 && reduce_cap >= h.n_reduce)
+      for (int i = 0; i < h.n_reduce; ++i) reduce4[4 * i + 3] = h.reduce[i].pad;
+    // the first five fields of every item at a stride of eight, the first three of every reduce entry at four
+    std::vector<int32_t> five(items8 && rc == MLA_OK && items_cap >= h.n_items ? (size_t)h.n_items * 5 : 0);
+    std::vector<int32_t> three(reduce4 && rc == MLA_OK && reduce_cap >= h.n_reduce ? (size_t)h.n_reduce * 3 : 0);
+    const int n_items = rc == MLA_OK ? h.n_items : 0, n_reduce = rc == MLA_OK ? h.n_reduce : 0;
     const int rc2 = export_host_plan(rc, h, counts4, five.empty() ? nullptr : five.data(), items_cap, work_indptr,
-                                     indptr_cap, reduce3, reduce_cap);
+                                     indptr_cap, three.empty() ? nullptr : three.data(), reduce_cap);
     if (rc2 == MLA_OK && !five.empty())
       for (int i = 0; i < n_items; ++i)
-        for (int f = 0; f < 5; ++f) items7[7 * i + f] = five[(size_t)i * 5 + f];
+        for (int f = 0; f < 5; ++f) items8[8 * i + f] = five[(size_t)i * 5 + f];
+    if (rc2 == MLA_OK && !three.empty())
+      for (int i = 0; i < n_reduce; ++i)
+        for (int f = 0; f < 3; ++f) reduce4[4 * i + f] = three[(size_t)i * 3 + f];
     return rc2;
   } catch (...) {
     return MLA_ERR_NOMEM;

@@ -19,7 +19,11 @@ constexpr int kVDim = MLA_V_HEAD_DIM;     // 512: value = first 512 entries of t
 // its final bf16 output. seq_len is the token count the plan saw, checked
 // against the device kv_indptr (and last page lengths); q_tok is the query
 // token's index within its sequence, checked against the device qo_indptr.
-// Single-token plans have q_row = b and q_tok = 0.
+// Single-token plans have q_row = b and q_tok = 0. pad is 0, except in
+// token-pair plans: there an item with pad >= 0 covers query rows q_row and
+// q_row + 1 (tokens q_tok, q_tok + 1), the first over [t_begin, pad), the
+// second over [t_begin, t_end), with partial slots slot and slot + 1; pad = -1
+// marks a single-token item (a sequence without KV rows).
 struct WorkItem {
   int32_t b;
   int32_t t_begin;
@@ -32,8 +36,8 @@ struct WorkItem {
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
-// One split query row for the reduce: slots [slot_begin, slot_begin + n_slots),
-// merged into output row b.
+// One split query row for the reduce: n_slots slots from slot_begin, pad apart
+// (0 or 1: consecutive; 2: a row of a token pair), merged into output row b.
 struct ReduceEntry {
   int32_t b;
   int32_t slot_begin;
@@ -49,6 +53,7 @@ struct HostPlan {
   int num_slots = 0;
   int64_t total_rows = 0;
   int64_t max_rows_per_cta = 0;
+  bool token_pairs = false;  // items are token pairs (see plan_tokens)
   WorkItem* items = nullptr;     // [n_items]
   int n_items = 0;
   int32_t* work_indptr = nullptr;  // [num_ctas + 1]
@@ -69,6 +74,7 @@ struct PlanOptions {
   int fp8_issuers = 0;  // tcgen05 kernel: 0 or 2 two MMA-issuing threads, 1 one issuer + three loaders
   int item_cost_rows = 256;  // balancing cost of each item a CTA starts, in KV rows (0 = none)
   bool token_parallel = true;  // multi-token plans with equal query counts: one CTA per (range, token)
+  bool token_pairs = false;    // multi-token plans with equal even query counts: tokens in pairs, one pass each
 };
 
 // Two MMA-issuing threads in the tcgen05 kernel unless asked for one: one
@@ -110,6 +116,7 @@ struct DevicePlan {
   int reduce_max_slots;  // most partial slots of any reduce entry (picks the reduce instance)
   int fp8_kernel;        // see PlanOptions
   int dual_issue;        // tcgen05 kernel instance: 1 two MMA issuers, 0 one
+  int token_pairs;       // the items are token pairs (only the fp8 tensor-core pair kernel takes them)
 };
 
 struct DecodeArgs {
@@ -184,5 +191,7 @@ int launch_reduce(void* out, const DevicePlan& p, void* stream, bool pdl);
 int launch_stage1_fp8_umma(const DecodeArgs& a, const DevicePlan& p, void* stream);
 // a16w8 on the tensor cores: the bf16 query as two e4m3 terms (stage1_umma_a16.cu).
 int launch_stage1_a16w8_umma(const DecodeArgs& a, const DevicePlan& p, void* stream);
+// fp8 stage 1 of a token-pair plan: both tokens of each item in one pass over its rows
+int launch_stage1_fp8_pairs_umma(const DecodeArgs& a, const DevicePlan& p, void* stream);
 
 }  // namespace mla

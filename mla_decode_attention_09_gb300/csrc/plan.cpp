@@ -36,6 +36,7 @@ PlanOptions resolve_options(const mla_plan_options* o) {
   if (o->item_cost_rows > 0) r.item_cost_rows = o->item_cost_rows;
   if (o->item_cost_rows < 0) r.item_cost_rows = 0;
   if (o->token_parallel < 0) r.token_parallel = false;
+  if (o->token_pairs > 0) r.token_pairs = true;
   return r;
 }
 
@@ -92,6 +93,14 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   // grid. They read the same rows at the same time: the rows come from HBM once
   // and from L2 for the other tokens (a range processing its tokens back to back
   // re-reads them from HBM once the ranges outgrow L2).
+  //
+  // Token pairs (opt-in): when that Q is even, query tokens 2v and 2v+1 of a
+  // sequence form one unit, processed in one pass over their rows by the fp8
+  // tensor-core kernel. A pair item covers rows [t_begin, t_end) for token
+  // 2v+1 and [t_begin, pad) for token 2v (pad >= t_begin), and its two partial
+  // slots are slot and slot + 1, so each row's slots lie two apart (the reduce
+  // entry's pad holds that stride). Sequences without KV rows keep one item
+  // per token, marked pad = -1.
   int64_t Qu = 0;
   bool uniform = true;
   for (int b = 0; b < batch; ++b) {
@@ -99,9 +108,13 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
     if (Qu == 0) Qu = n_queries(b);
     else if (n_queries(b) != Qu) uniform = false;
   }
-  const bool token_par = opt.token_parallel && uniform && Qu > 1 && max_ctas / Qu >= 1;
-  if (token_par) max_ctas /= Qu;
-  auto weight = [&](int b) { return token_par ? (int64_t)1 : n_queries(b); };  // query tokens per range
+  const bool pairs = opt.token_pairs && uniform && Qu >= 2 && Qu % 2 == 0;
+  out->token_pairs = pairs;
+  const int64_t Qn = pairs ? Qu / 2 : Qu;  // query units (tokens, or token pairs) of a sequence with rows
+  const bool token_par = opt.token_parallel && uniform && Qn > 1 && max_ctas / Qn >= 1;
+  if (token_par) max_ctas /= Qn;
+  // query units per range
+  auto weight = [&](int b) { return token_par ? (int64_t)1 : pairs ? n_queries(b) / 2 : n_queries(b); };
   int64_t U = 0, n_pieces_min = 0;
   for (int b = 0; b < batch; ++b) {
     U += ngran[(size_t)b] * weight(b);
@@ -166,31 +179,45 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   items.reserve((size_t)qo[(size_t)batch] + ranges.size() * 2);
   size_t cta = 0;  // range index
   const size_t last = ranges.size() - 1;
-  auto push = [&](int b, int64_t t0, int64_t t1, int64_t j) {
+  // unit: the query token (or pair) index that picks the CTA of a token-parallel range
+  auto push = [&](int b, int64_t t0, int64_t t1, int64_t j, int64_t unit, int64_t pad) {
     items.push_back(WorkItem{b, (int32_t)t0, (int32_t)t1, -1, (int32_t)seq_len(b), (int32_t)(qo[(size_t)b] + j),
-                             (int32_t)j, 0});
-    // token-parallel: token j's CTA of the range. Only a sequence without KV rows can
-    // have more than Qu tokens (its items write zeros); they go to the range's last CTA.
-    cta_of_item.push_back((int32_t)(token_par ? (int64_t)cta * Qu + std::min<int64_t>(j, Qu - 1) : (int64_t)cta));
+                             (int32_t)j, (int32_t)pad});
+    // token-parallel: the unit's CTA of the range. Only a sequence without KV rows can
+    // have more than Qn units (its items write zeros); they go to the range's last CTA.
+    cta_of_item.push_back((int32_t)(token_par ? (int64_t)cta * Qn + std::min<int64_t>(unit, Qn - 1) : (int64_t)cta));
   };
   for (int b = 0; b < batch; ++b) {
     const int64_t S = tok[(size_t)b], E = tok[(size_t)b + 1], q_b = n_queries(b);
     while (cta < last && ranges[cta].second <= S) ++cta;
-    // query tokens that see no KV token write zeros (a zero-row item)
-    for (int64_t j = 0; j < q_b; ++j)
-      if (visible(b, j) == 0) push(b, 0, 0, j);
+    const bool pair_seq = pairs && S < E;  // a sequence with rows: its q_b is the even Qu
+    // query tokens that see no KV token write zeros (a zero-row item; a pair when neither token sees one)
+    if (pair_seq) {
+      for (int64_t v = 0; v < q_b / 2; ++v)
+        if (visible(b, 2 * v + 1) == 0) push(b, 0, 0, 2 * v, v, 0);
+    } else {
+      for (int64_t j = 0; j < q_b; ++j)
+        if (visible(b, j) == 0) push(b, 0, 0, j, j, pairs ? -1 : 0);
+    }
     if (S == E || q_b == 0) continue;
     while (true) {
       const int64_t a = std::max(S, ranges[cta].first) - S, e = std::min(E, ranges[cta].second) - S;
-      for (int64_t j = 0; j < q_b; ++j) {  // the query tokens of this row range, back to back
-        const int64_t ej = std::min(e, visible(b, j));
-        if (ej > a) push(b, a, ej, j);
+      if (pair_seq) {
+        for (int64_t v = 0; v < q_b / 2; ++v) {  // token 2v+1 sees at least the rows token 2v sees
+          const int64_t e1 = std::min(e, visible(b, 2 * v + 1));
+          if (e1 > a) push(b, a, e1, 2 * v, v, std::max(a, std::min(e, visible(b, 2 * v))));
+        }
+      } else {
+        for (int64_t j = 0; j < q_b; ++j) {  // the query tokens of this row range, back to back
+          const int64_t ej = std::min(e, visible(b, j));
+          if (ej > a) push(b, a, ej, j, j, 0);
+        }
       }
       if (E <= ranges[cta].second || cta == last) break;
       ++cta;
     }
   }
-  const int64_t used_ctas = (int64_t)ranges.size() * (token_par ? Qu : 1);
+  const int64_t used_ctas = (int64_t)ranges.size() * (token_par ? Qn : 1);
   if (token_par) {  // group the items by CTA, keeping each CTA's items (and each row's pieces) in order
     std::vector<size_t> order(items.size());
     for (size_t i = 0; i < order.size(); ++i) order[i] = i;
@@ -206,20 +233,34 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   }
 
   // Partial slots for query rows cut into several items, consecutive per row, rows in order.
+  // A pair's two rows have the same items; their slots interleave (stride 2).
   const size_t n_rows = (size_t)qo[(size_t)batch];
+  auto is_pair = [&](const WorkItem& w) { return pairs && w.pad >= 0; };
   std::vector<int32_t> count(n_rows, 0), next(n_rows, 0);
-  for (const WorkItem& w : items) count[(size_t)w.q_row]++;
+  std::vector<char> second(n_rows, 0);  // the second row of a pair
+  for (const WorkItem& w : items) {
+    count[(size_t)w.q_row]++;
+    if (is_pair(w)) second[(size_t)w.q_row + 1] = 1;
+  }
   std::vector<ReduceEntry> reduce;
   int slot = 0;
   for (size_t r = 0; r < n_rows; ++r) {
-    if (count[r] > 1) {
+    if (count[r] <= 1 || second[r]) continue;
+    next[r] = slot;
+    if (r + 1 < n_rows && second[r + 1]) {
+      reduce.push_back(ReduceEntry{(int32_t)r, slot, count[r], 2});
+      reduce.push_back(ReduceEntry{(int32_t)r + 1, slot + 1, count[r], 2});
+      slot += 2 * count[r];
+    } else {
       reduce.push_back(ReduceEntry{(int32_t)r, slot, count[r], 0});
-      next[r] = slot;
       slot += count[r];
     }
   }
   for (WorkItem& w : items)
-    if (count[(size_t)w.q_row] > 1) w.slot = next[(size_t)w.q_row]++;
+    if (count[(size_t)w.q_row] > 1) {
+      w.slot = next[(size_t)w.q_row];
+      next[(size_t)w.q_row] += is_pair(w) ? 2 : 1;
+    }
 
   // Items are already grouped by CTA in increasing order: CSR offsets.
   for (int32_t c : cta_of_item)

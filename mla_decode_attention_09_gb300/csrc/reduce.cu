@@ -47,7 +47,9 @@ __global__ void __launch_bounds__(kReduceThreads)
   const int lane = threadIdx.x & 31;
   const int n = r.n_slots;
   const float* lse = p.part_lse + (int64_t)r.slot_begin * kHeads + h;
-  constexpr int64_t kSlotStride = (int64_t)kHeads * kVDim;
+  // the row's slots lie r.pad apart (token pairs interleave theirs), else consecutively
+  const int64_t lse_stride = (int64_t)max(r.pad, 1) * kHeads;
+  const int64_t kSlotStride = lse_stride * kVDim;
   const float* po = p.part_o + ((int64_t)r.slot_begin * kHeads + h) * kVDim + 4 * threadIdx.x;
   auto warp_max = [](float x) {
 #pragma unroll
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(kReduceThreads)
   };
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (n <= kBatch) {
-    const float ls = lane < n ? lse[(int64_t)lane * kHeads] : -INFINITY;
+    const float ls = lane < n ? lse[lane * lse_stride] : -INFINITY;
     float4 v[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u)
@@ -75,16 +77,16 @@ __global__ void __launch_bounds__(kReduceThreads)
     }
   } else {
     float m = -INFINITY;
-    for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[(int64_t)s * kHeads]);
+    for (int s = lane; s < n; s += 32) m = fmaxf(m, lse[s * lse_stride]);
     m = warp_max(m);
     if (m != -INFINITY) {
       float z = 0.f;
-      for (int s = lane; s < n; s += 32) z += exp2f(lse[(int64_t)s * kHeads] - m);
+      for (int s = lane; s < n; s += 32) z += exp2f(lse[s * lse_stride] - m);
       const float inv_z = 1.0f / warp_sum(z);
       for (int s0 = 0; s0 < n; s0 += kBatch) {
         // lane j holds the weight of slot s0 + j
         const int cnt = min(kBatch, n - s0);
-        const float wl = lane < cnt ? exp2f(lse[(int64_t)(s0 + lane) * kHeads] - m) * inv_z : 0.f;
+        const float wl = lane < cnt ? exp2f(lse[(s0 + lane) * lse_stride] - m) * inv_z : 0.f;
         float4 v[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)

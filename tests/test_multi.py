@@ -116,3 +116,90 @@ def test_multi_full_size(mla, k8):
     assert plan.check_error() == 0
     # every query row, element by element
     compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, "multi full size")
+
+
+# ---------------------------------------------------------------- token pairs (fp8, tensor cores)
+# Plans made with token_pairs = 1 take query tokens 2v and 2v+1 of a sequence in one pass over
+# their rows (mla_decode_attention_09_gb300/csrc/stage1_umma_pairs.cu).
+PAIRS = {"token_pairs": 1}
+
+
+def pair_items(mla, qo, inp, num_sms, causal, **opts):
+    """The host planner's items for the same request (no GPU): checks what a case exercises."""
+    return mla.plan_compute_host_multi(qo, inp.kv_indptr, num_sms, causal=causal, page_size=inp.page_size,
+                                       kv_last_page_len_host=inp.kv_last_page_len, token_pairs=1, **opts)["items"]
+
+
+@pytest.mark.parametrize("qn", [2, 4])
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+@pytest.mark.parametrize("split", ["whole", "split"])
+@pytest.mark.parametrize("layout", ["rows", "pages64", "pages8"])
+def test_token_pairs(mla, qn, causal, split, layout):
+    lengths = [1, 2, 3, 130, 640, 1000, 3 * 128 + 5, 7 * 128, 2000, 65]
+    mode = mi.MODE_FP8
+    seed = 400 + qn + (10 if causal else 0)
+    if layout == "rows":
+        inp = mi.make_inputs(lengths, mode, seed=seed, permute=True, extra_slots=7)
+    else:
+        inp = mi.make_paged_inputs(lengths, 64 if layout == "pages64" else 8, mode, seed=seed, permute=True,
+                                   extra_pages=3)
+    q, qo = mi.make_query_tokens([qn] * len(lengths), seed=seed + 1, q_std=2.0)
+    opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
+    num_sms = 152 if split == "whole" else 12
+    items = pair_items(mla, qo, inp, num_sms, causal, **opts)
+    assert (items[:, 7] >= 0).all()  # a pair plan
+    out, plan = run_multi(mla, inp, q, qo, causal, num_sms=num_sms, **PAIRS, **opts)
+    assert plan.check_error() == 0
+    if split == "split":
+        assert plan.info()["num_split_seqs"] > 0
+    compare(out, oracle_multi(inp, q, qo, causal), mode, f"token pairs q={qn} {layout} {split} causal={causal}")
+
+
+@pytest.mark.parametrize("q_std", [1.0, 3.0])
+def test_token_pairs_sharp_softmax(mla, q_std):
+    lengths = [2000, 1000, 4096, 130, 7]
+    inp = mi.make_inputs(lengths, mi.MODE_FP8, seed=430, permute=True, extra_slots=5)
+    q, qo = mi.make_query_tokens([2] * len(lengths), seed=431, q_std=q_std)
+    out, plan = run_multi(mla, inp, q, qo, True, num_sms=20, **PAIRS)
+    assert plan.check_error() == 0
+    compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, f"token pairs q_std={q_std}")
+
+
+def test_token_pairs_edge_items(mla):
+    """Pieces where the first token of a pair sees none of the rows (its causal prefix ends at the
+    piece's start), whole items where it sees nothing at all, and sequences without rows that hold
+    an odd number of query tokens (single-token items writing zeros)."""
+    lengths, q_lens = [65, 129, 1, 2, 0, 0], [2, 2, 2, 2, 3, 0]
+    inp = mi.make_inputs(lengths, mi.MODE_FP8, seed=440, permute=True, extra_slots=3)
+    q, qo = mi.make_query_tokens(q_lens, seed=441, q_std=2.0)
+    opts = {"min_rows_per_split": 16, "granularity": 16, "item_cost_rows": -1}
+    items = pair_items(mla, qo, inp, 20, True, **opts)
+    pair = items[:, 7]
+    assert ((pair >= 0) & (pair == items[:, 1]) & (items[:, 2] > items[:, 1]) & (items[:, 3] >= 0)).sum() >= 2
+    assert ((pair >= 0) & (pair == items[:, 1]) & (items[:, 2] > items[:, 1]) & (items[:, 3] < 0)).sum() >= 1
+    assert (pair < 0).sum() == 3
+    out, plan = run_multi(mla, inp, q, qo, True, num_sms=20, **PAIRS, **opts)
+    assert plan.check_error() == 0
+    compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, "token pairs edge items")
+
+
+def test_token_pairs_need_the_fp8_tensor_core_kernel(mla):
+    inp = mi.make_inputs([300, 40], mi.MODE_BF16, seed=450)
+    q, qo = mi.make_query_tokens([2, 2], seed=451)
+    d = inp.to("cuda")
+    out = torch.zeros((4, 16, 512), dtype=torch.bfloat16, device="cuda")
+    for mode, extra in ((mi.MODE_BF16, {}), (mi.MODE_A16W8, {}), (mi.MODE_FP8, {"fp8_kernel": 1})):
+        plan = mla.plan_multi(qo, inp.kv_indptr, causal=True, **PAIRS, **extra)
+        with pytest.raises(mla.MLAError) as e:
+            mla.decode_multi(q.cuda(), d.kv, torch.ones(1, device="cuda"), qo.cuda(), d.kv_indptr, d.kv_indices, out,
+                             plan=plan, dtype_mode=mode)
+        assert e.value.status == -1
+
+
+@pytest.mark.parametrize("qn", [2, 4])
+def test_token_pairs_full_size(mla, qn):
+    inp = mi.make_workload("fp8_b64_l8192")
+    q, qo = mi.make_query_tokens([qn] * 64, seed=92 + qn)
+    out, plan = run_multi(mla, inp, q, qo, True, **PAIRS)
+    assert plan.check_error() == 0
+    compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, f"token pairs full size q={qn}")

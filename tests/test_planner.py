@@ -225,11 +225,11 @@ def test_multi_plan_covers_every_query_token(causal, num_sms, opts):
     items, wip, red = r["items"], r["work_indptr"], r["reduce"]
     assert wip[0] == 0 and wip[-1] == len(items)
     by_row = {}
-    for b, t0, t1, slot, L, q_row, q_tok in items:
+    for b, t0, t1, slot, L, q_row, q_tok, _pair in items:
         assert L == lengths[b] and q_row == qo[b] + q_tok and 0 <= q_tok < q_lens[b]
         by_row.setdefault(int(q_row), []).append((int(t0), int(t1), int(slot)))
     assert sorted(by_row) == list(range(int(qo[-1])))  # every query row is produced
-    red_map = {int(rw): (int(s0), int(n)) for rw, s0, n in red}
+    red_map = {int(rw): (int(s0), int(n)) for rw, s0, n, _stride in red}
     for b in range(len(lengths)):
         for j in range(q_lens[b]):
             parts = by_row[int(qo[b]) + j]
@@ -259,7 +259,8 @@ def test_multi_plan_with_one_query_token_is_the_row_plan():
         m = mla.plan_compute_host_multi(qo, ip, 9, causal=causal, min_rows_per_split=16, granularity=16)
         r = mla.plan_compute_host(ip, 9, min_rows_per_split=16, granularity=16)
         assert np.array_equal(m["items"][:, :5], r["items"])
-        assert np.array_equal(m["work_indptr"], r["work_indptr"]) and np.array_equal(m["reduce"], r["reduce"])
+        assert np.array_equal(m["work_indptr"], r["work_indptr"]) and np.array_equal(m["reduce"][:, :3], r["reduce"])
+        assert not m["items"][:, 7].any() and not m["reduce"][:, 3].any()
 
 
 def test_multi_plan_balances_weighted_granules():
@@ -348,7 +349,7 @@ def test_multi_plan_token_parallel_random():
         assert 1 <= r["num_ctas"] <= max(num_sms, 1) and wip[0] == 0 and wip[-1] == len(items)
         assert np.all(np.diff(wip) >= 0)
         by_row = {}
-        for b, t0, t1, slot, L, q_row, q_tok in items:
+        for b, t0, t1, slot, L, q_row, q_tok, _pair in items:
             assert L == lengths[b] and q_row == qo[b] + q_tok
             by_row.setdefault(int(q_row), []).append((int(t0), int(t1)))
         assert sorted(by_row) == list(range(int(qo[-1])))
@@ -361,3 +362,119 @@ def test_multi_plan_token_parallel_random():
                     assert t0 == pos
                     pos = t1
                 assert pos == n
+
+
+def _pair_rows(items):
+    """Expand a token-pair plan's items into per-query-row parts (first token, end token, slot)."""
+    by_row = {}
+    for b, t0, t1, slot, L, q_row, q_tok, pair in (tuple(int(v) for v in x) for x in items):
+        if pair >= 0:  # rows q_row (token q_tok, over [t0, pair)) and q_row + 1 (over [t0, t1))
+            assert t0 <= pair <= t1 or t1 == t0 == 0
+            by_row.setdefault(q_row, []).append((t0, min(pair, t1), slot))
+            by_row.setdefault(q_row + 1, []).append((t0, t1, slot + 1 if slot >= 0 else -1))
+        else:
+            by_row.setdefault(q_row, []).append((t0, t1, slot))
+    return by_row
+
+
+def _check_pair_plan(lengths, q_lens, num_sms, causal, **opts):
+    ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+    ip[1:] = np.cumsum(lengths)
+    qo = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    qo[1:] = np.cumsum(q_lens)
+    r = mla.plan_compute_host_multi(qo, ip, num_sms, causal=causal, token_pairs=1, **opts)
+    items, wip, red = r["items"], r["work_indptr"], r["reduce"]
+    counts = {q for L, q in zip(lengths, q_lens) if L > 0 and q > 0}
+    if len(counts) != 1 or min(counts) % 2:  # not a pair plan: the ordinary one
+        plain = mla.plan_compute_host_multi(qo, ip, num_sms, causal=causal, **opts)
+        assert all(np.array_equal(r[k], plain[k]) for k in ("items", "work_indptr", "reduce"))
+        return r
+    assert wip[0] == 0 and wip[-1] == len(items) and np.all(np.diff(wip) >= 0)
+    assert 1 <= r["num_ctas"] <= num_sms * opts.get("ctas_per_sm", 1)
+    for x in items:
+        b, q_row, q_tok, pair = int(x[0]), int(x[5]), int(x[6]), int(x[7])
+        assert q_row == qo[b] + q_tok and int(x[4]) == lengths[b]
+        if pair >= 0:  # a pair starts at an even token of a sequence with rows
+            assert q_tok % 2 == 0 and q_tok + 1 < q_lens[b] and lengths[b] > 0
+        else:
+            assert lengths[b] == 0 and int(x[2]) == int(x[1]) == 0
+    by_row = _pair_rows(items)
+    assert sorted(by_row) == list(range(int(qo[-1])))  # every query row is produced
+    red_map = {int(rw): (int(s0), int(n), int(st)) for rw, s0, n, st in red}
+    used = []
+    for b in range(len(lengths)):
+        for j in range(q_lens[b]):
+            row = int(qo[b]) + j
+            parts = by_row[row]
+            n = _visible(lengths[b], q_lens[b], j, causal)
+            pos = 0
+            for t0, t1, _ in parts:  # the non-empty parts cover the visible tokens in order
+                if t1 > t0:
+                    assert t0 == pos
+                    pos = t1
+            assert pos == n
+            if len(parts) == 1:
+                assert parts[0][2] == -1 and row not in red_map
+            else:
+                s0, cnt, st = red_map[row]
+                assert cnt == len(parts) and st == 2
+                assert [p[2] for p in parts] == list(range(s0, s0 + 2 * cnt, 2))
+                used += [p[2] for p in parts]
+    assert sorted(used) == list(range(r["num_slots"]))  # every slot written once
+    return r
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("Q", [2, 4, 6])
+def test_pair_plan_covers_every_query_token(causal, Q):
+    """Token pairs: an item covers tokens 2v (over [t_begin, pair field)) and 2v+1 (over [t_begin,
+    end)); each row's slots lie two apart; ranges are token-parallel over the Q/2 pairs."""
+    B, L = 16, 3000
+    r = _check_pair_plan([L] * B, [Q] * B, 40, causal)
+    items, wip = r["items"], r["work_indptr"]
+    U = Q // 2
+    assert r["num_ctas"] % U == 0
+    assert (items[:, 7] >= 0).all()
+    for rg in range(r["num_ctas"] // U):
+        for v in range(U):
+            assert all(int(x[6]) == 2 * v for x in items[wip[rg * U + v]:wip[rg * U + v + 1]])
+
+
+def test_pair_plan_edge_lengths():
+    """Sequences shorter than their query count (tokens that see nothing), one-row sequences,
+    sequences without rows holding any number of tokens, and ranges that hold only the last row."""
+    for causal in (True, False):
+        _check_pair_plan([1, 2, 3, 0, 129, 0, 64, 65], [2, 2, 2, 3, 2, 0, 2, 2], 5, causal,
+                         min_rows_per_split=16, granularity=16)
+        _check_pair_plan([4096, 4, 0, 8193], [4, 4, 5, 4], 3, causal, min_rows_per_split=16, granularity=16)
+        _check_pair_plan([65, 65], [2, 2], 8, causal, min_rows_per_split=16, granularity=16, item_cost_rows=-1)
+
+
+def test_pair_plan_needs_equal_even_counts():
+    lengths = [500, 600, 700]
+    ip = np.zeros(4, dtype=np.int32)
+    ip[1:] = np.cumsum(lengths)
+    for q_lens in ([3, 3, 3], [2, 4, 2], [1, 1, 1]):
+        qo = np.zeros(4, dtype=np.int32)
+        qo[1:] = np.cumsum(q_lens)
+        on = mla.plan_compute_host_multi(qo, ip, 20, causal=True, token_pairs=1)
+        off = mla.plan_compute_host_multi(qo, ip, 20, causal=True)
+        assert not on["items"][:, 7].any() and not on["reduce"][:, 3].any()
+        for k in ("items", "work_indptr", "reduce"):
+            assert np.array_equal(on[k], off[k])
+
+
+def test_pair_plan_random():
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        B = int(rng.integers(1, 24))
+        Q = int(rng.choice([2, 4, 6, 8]))
+        lengths = [int(x) for x in rng.integers(0, 3000, B)]
+        for k in range(B):
+            if rng.random() < 0.15:
+                lengths[k] = int(rng.integers(0, 4))
+        q_lens = [Q if L > 0 else int(rng.integers(0, 9)) for L in lengths]
+        opts = {"min_rows_per_split": 16, "granularity": 16} if rng.random() < 0.5 else {}
+        if rng.random() < 0.3:
+            opts["token_parallel"] = -1
+        _check_pair_plan(lengths, q_lens, int(rng.integers(1, 160)), bool(rng.random() < 0.8), **opts)
