@@ -86,6 +86,21 @@ def test_odd_lengths(mla, mode, k8, split):
     compare(out, oracle_out(inp), mode, f"odd lengths {split}")
 
 
+@pytest.mark.parametrize("k8", [{}, {"fp8_kernel": 1}], ids=["a16w8-tcgen05", "a16w8-mma"])
+@pytest.mark.parametrize("q_std", [1.0, 2.0])
+def test_a16w8_keeps_the_bf16_query(mla, k8, q_std):
+    # The same inputs decoded as fp8 (query cast to e4m3) differ from the a16w8 definition by more
+    # than the bf16 tolerance, so a kernel that rounded the query to one e4m3 term would fail here.
+    inp = mi.make_inputs([300, 1000, 37, 2048], mi.MODE_A16W8, seed=700, permute=True, extra_slots=9, q_std=q_std)
+    ref = oracle_out(inp)
+    as_fp8, _ = oracle.decode(inp.q, inp.kv, inp.kv_indptr, inp.kv_indices, inp.sm_scale, mi.MODE_FP8, inp.kv_scale)
+    gap = np.linalg.norm(as_fp8 - ref) / np.linalg.norm(ref)
+    assert gap > 2 * TOL[mi.MODE_A16W8][1], f"test inputs do not separate the modes (rel-L2 {gap:.2e})"
+    out, plan = run(mla, inp, num_sms=20, **k8)
+    assert plan.check_error() == 0
+    compare(out, ref, mi.MODE_A16W8, f"a16w8 q_std={q_std}")
+
+
 @pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
 def test_one_long_sequence_many_splits(mla, mode, k8):
     inp = mi.make_inputs([5003], mode, seed=7)
