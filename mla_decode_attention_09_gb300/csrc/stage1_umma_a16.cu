@@ -57,7 +57,6 @@ constexpr int kLatStages = 3;
 // B operand of N = 32 columns whose second 16-column group lies kPLo further on.
 constexpr int kPLo = kRowsU * 16;             // 2 KB
 constexpr int kPBuf = 2 * kPLo;               // 4 KB per buffer
-constexpr uint32_t kTileTx = kLatStage + kRopeStage;
 constexpr int kThreadsU = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                 // S^T: 2 buffers x 32 columns (hi, lo)
@@ -79,7 +78,8 @@ constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 32, 1, 1);
 constexpr uint32_t kLayoutSw64 = 4;
 
 enum : int {
-  kBFull = 0,     // [3] tile data landed (TMA tx, and every loader lane's cp.async arrival)
+  kBFull = 0,     // [3] latent part of a tile landed, and the rope part in the paged instance (TMA tx, and
+                  //     every loader lane's cp.async arrival)
   kBLEmpty = 3,   // [3] latent slot free (P.V done)
   kBREmpty = 6,   // [2] rope slot free (the tile's P.V done: the slot held its P)
   kBSFull = 8,    // [2] S^T ready
@@ -89,7 +89,8 @@ enum : int {
   kBQEmpty = 15,  // query consumed (last scores of the item done)
   kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals)
   kBDrain = 18,   // every MMA of the CTA done (both issuing threads commit)
-  kNumBars = 19
+  kBRFull = 19,   // [2] rope part of a tile landed, row instance (TMA tx, and every loader lane's arrival)
+  kNumBars = 21
 };
 
 // The query as two e4m3 terms of 16 heads each: a 32-row B matrix. Each tile's
@@ -283,6 +284,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((int)blockIdx.x >= p.num_ctas) return;
   constexpr int kLoaders = 2;  // tiles copied row by row are split between warps 4 and 7
+  // row instance: a tile's latent and rope parts land on separate barriers
+  constexpr bool kSplit = !kPaged;
 
   // 1024-aligned base for the swizzle atoms
   // The swizzle atoms need 1024-aligned buffers and the allocation has no room to
@@ -306,6 +309,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       ptx::mbar_init(bar(kBLEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(kBRFull + i), 1 + 32 * kLoaders);
       ptx::mbar_init(bar(kBREmpty + i), 1);
       ptx::mbar_init(bar(kBSFull + i), 1);
       ptx::mbar_init(bar(kBPFull + i), 128);
@@ -350,9 +354,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const float kv_scale = __ldg(a.kv_scale);
   const float score_log2 = a.sm_scale * kv_scale * kLog2eU;
 
-  // MMA issue of one tile (one thread): scores, and P.V
-  auto issue_qk = [&](const TCur& c, int i) {
-    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, rope = rope_addr + (i & 1) * kRopeStage;
+  // MMA issue of one tile (one thread): scores over the latent dims (once the
+  // latent part has landed), then over the rope dims (once the rope part has:
+  // its slot is the last to free), and P.V
+  auto issue_qk_lat = [&](int i) {
+    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage;
     const uint32_t d = tmem + kColS + (uint32_t)kNQ * (uint32_t)(i & 1);
     umma::fence_after_sync();
     // row-copied tile: order the cp.async (generic proxy) writes before the tensor core reads them
@@ -363,6 +369,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       umma::mma_f8f6f4(d, umma::smem_desc(lat + kb * kBlk + ko, 16, 1024, umma::kLayoutSw128),
                        umma::smem_desc(q_addr + kb * kQKBlk + ko, 16, 1024, umma::kLayoutSw128), kIdescQK, st > 0);
     }
+  };
+  auto issue_qk_rope = [&](const TCur& c, int i) {
+    const uint32_t rope = rope_addr + (i & 1) * kRopeStage;
+    const uint32_t d = tmem + kColS + (uint32_t)kNQ * (uint32_t)(i & 1);
+    umma::fence_after_sync();
+    if (row_copy[i % kLatStages]) umma::fence_proxy_async_smem();
 #pragma unroll
     for (int st = 0; st < 2; ++st)
       umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
@@ -452,9 +464,36 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int run_ps = (kPaged && page_boxes(a.page_size)) ? a.page_size : 0;
     int nruns = 0, run_y = oob_row;
     IdleClock idle;
-    while (!c.done) {
+    // Row instance (kSplit): a tile of consecutive rows has its latent part
+    // issued once its latent slot is free, and its rope part, on its own barrier,
+    // once its rope slot is free too. That slot holds the P of the tile two before
+    // until its P.V is done, later than the latent slot frees, and the scores over
+    // the latent dims need not wait for it. The main loader keeps at most one
+    // tile's rope part pending. Tiles copied row by row take both slots at once.
+    // The paged instance loads both parts together on one barrier: split, it
+    // measured slower.
+    auto issue_rope = [&](int t, int y) {  // main loader, whole warp
+      const uint32_t rb = bar(kBRFull + (t & 1)), rope = rope_addr + (t & 1) * kRopeStage;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(rb, kRopeStage);
+        umma::tma_load_2d(rope, &tm.rope_tile, 512, y, rb, pol);
+      }
+      umma::cp_async_arrive_noinc(rb);
+    };
+    bool pend = false;
+    int pend_i = 0, pend_y = oob_row;
+    while (!c.done || pend) {
       bool progress = false;
-      if (!c.done) {
+      if (pend) {  // main loader of the row instance only
+        bool rfree = pend_i < 2 || ptx::mbar_test_wait(bar(kBREmpty + (pend_i & 1)), ((pend_i >> 1) - 1) & 1);
+        rfree = __shfl_sync(~0u, rfree, 0);
+        if (rfree) {
+          issue_rope(pend_i, pend_y);
+          pend = false;
+          progress = true;
+        }
+      }
+      if (!c.done && !pend) {
         const int ls = i % kLatStages, rs = i & 1;
         const int nv = c.t_end - c.t0;
         if (!decided) {
@@ -484,16 +523,19 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           }
           decided = true;
         }
-        bool ready;
-        if (main_loader) {  // polls: it also stages queries
+        const bool row_copied = !cont && !runs;  // both parts copied row by row, at once
+        bool ready, rope_ready = true;
+        if (main_loader) {  // polls
           ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
           // the rope slot is free once P.V of the tile two before is done
-          ready = ready && (i < 2 || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
+          rope_ready = i < 2 || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1);
+          if (!kSplit || !cont) ready = ready && rope_ready;
           ready = __shfl_sync(~0u, ready, 0);
+          rope_ready = __shfl_sync(~0u, rope_ready, 0);
         } else {  // the extra loaders have nothing else to do: a bounded blocking wait
           const bool w_ok =
               (i < kLatStages || wait_u(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1, abort_flag)) &&
-              (i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag));
+              ((kSplit && cont) || i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag));
           if (!__all_sync(~0u, w_ok)) {
             ok = false;
             break;
@@ -501,10 +543,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           ready = true;
         }
         if (ready) {
-          const uint32_t fb = bar(kBFull + ls);
+          const uint32_t fb = bar(kBFull + ls), rb = bar(kBRFull + rs);
           const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
-          if (main_loader && lane == 0) row_copy[ls] = (cont || runs) ? 0 : 1;  // published by the arrivals below
-          if (runs) {
+          if (main_loader && lane == 0) row_copy[ls] = row_copied ? 1 : 0;  // published by the arrivals below
+          if (runs) {  // the paged instance only: both parts on the latent barrier
             if (main_loader) {
               if (lane == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)(nruns * run_ps * kQkDim));
               __syncwarp();
@@ -517,10 +559,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
           } else if (cont) {
             if (main_loader) {
-              if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kTileTx);
+              if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kSplit ? kLatStage : kLatStage + kRopeStage);
               __syncwarp();
               if (lane < 4) umma::tma_load_2d(lat + lane * kBlk, &tm.lat_tile, lane * 128, y0, fb, pol);
-              if (lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
+              if (!kSplit && lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
             }
           } else {
             // Row r's index sits in lane (r & 31), slot (r >> 5); loader g of n copies the
@@ -551,9 +593,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
               umma::cp_async_16(dst, kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 512 + 16 * (lane & 3),
                                 valid ? 16u : 0u, pol);
             }
-            if (main_loader && lane == 0) umma::mbar_arrive(fb);
+            if (main_loader && lane == 0) {
+              umma::mbar_arrive(fb);
+              if (kSplit) umma::mbar_arrive(rb);
+            }
           }
           umma::cp_async_arrive_noinc(fb);
+          if constexpr (kSplit) {
+            if (row_copied) {
+              umma::cp_async_arrive_noinc(rb);
+            } else if (main_loader) {
+              if (rope_ready) {
+                issue_rope(i, y0);
+              } else {
+                pend = true;
+                pend_i = i;
+                pend_y = y0;
+              }
+            } else {  // the extra loader arrives on the rope barrier once the rope slot is free
+              const bool r_ok = i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag);
+              if (!__all_sync(~0u, r_ok)) {
+                ok = false;
+                break;
+              }
+              umma::cp_async_arrive_noinc(rb);
+            }
+          }
           // shift the index pipeline: tile i+1's indices are already loaded, request tile i+2's
 #pragma unroll
           for (int j = 0; j < 4; ++j) y0s[j] = y1s[j];
@@ -582,6 +647,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       if (ptx::mbar_try_wait(b_, par)) continue;
       (void)ptx::mbar_wait_bounded(b_, par, kDrainLimitNsU);
     }
+    for (int t = (i >= 2 ? i - 2 : 0); kSplit && main_loader && t < i; ++t) {
+      const uint32_t b_ = bar(kBRFull + (t & 1));
+      const uint32_t par = (uint32_t)(t >> 1) & 1u;
+      if (ptx::mbar_try_wait(b_, par)) continue;
+      (void)ptx::mbar_wait_bounded(b_, par, kDrainLimitNsU);
+    }
   } else if (warp == 5) {
     // ------------------------------------------------ score MMAs (one thread)
     // Scores of tile j need the item's query (first tile), the tile's data, and
@@ -596,7 +667,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
              wait_u(bar(kBFull + nq % kLatStages), (nq / kLatStages) & 1, abort_flag) &&
              (nq < 2 || wait_u(bar(kBPFull + (nq & 1)), ((nq - 2) >> 1) & 1, abort_flag));
         if (!ok) break;
-        issue_qk(c, nq);
+        issue_qk_lat(nq);
+        if constexpr (kSplit) {  // the rope part has its own barrier
+          ok = wait_u(bar(kBRFull + (nq & 1)), (nq >> 1) & 1, abort_flag);
+          if (!ok) break;
+        }
+        issue_qk_rope(c, nq);
         ++nq;
         tcur_next<kPaged>(c, p, a);
       }
