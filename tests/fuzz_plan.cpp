@@ -75,6 +75,7 @@ int main(int argc, char** argv) {
     o.ctas_per_sm = (int)U(1, 3);
     o.item_cost_rows = (int)std::vector<int64_t>{0, 1, 256, 100000}[U(0, 3)];
     o.token_parallel = U(0, 1) == 1;
+    o.token_pairs = U(0, 1) == 1;
     const int num_sms = (int)U(1, 300);
     const int ps = (int)std::vector<int64_t>{1, 2, 3, 8, 64, 128, 1000}[U(0, 6)];
     std::vector<int32_t> ip(B + 1, 0), last(B, 1), qo(B + 1, 0);
@@ -101,9 +102,19 @@ int main(int argc, char** argv) {
     for (int i = 0; i < h.n_items; ++i) {
       const WorkItem& w = h.items[i];
       if (w.slot >= h.num_slots || w.t_begin > w.t_end || w.t_begin < 0) { printf("bad item\n"); return 1; }
+      // a token pair writes slots slot and slot + 1, and its first token's rows end within the item's
+      if (h.token_pairs && w.pad >= 0) {
+        if (w.slot >= 0 && w.slot + 1 >= h.num_slots) { printf("bad pair slot\n"); return 1; }
+        if (w.t_end > w.t_begin && (w.pad < w.t_begin || w.pad > w.t_end)) { printf("bad pair end\n"); return 1; }
+      }
     }
-    for (int r = 0; r < h.n_reduce; ++r)
-      if (h.reduce[r].slot_begin < 0 || h.reduce[r].slot_begin + h.reduce[r].n_slots > h.num_slots) { printf("bad reduce\n"); return 1; }
+    for (int r = 0; r < h.n_reduce; ++r) {  // slots slot_begin + k * stride, k < n_slots
+      const int stride = h.reduce[r].pad > 1 ? h.reduce[r].pad : 1;
+      if (h.reduce[r].slot_begin < 0 || h.reduce[r].slot_begin + stride * (h.reduce[r].n_slots - 1) >= h.num_slots) {
+        printf("bad reduce\n");
+        return 1;
+      }
+    }
     if (kind == 0) {
       const char* e = check_rows(B, ip.data(), h.items, h.n_items, h.work_indptr, h.num_ctas, h.reduce, h.n_reduce,
                                  h.num_slots);
