@@ -58,7 +58,7 @@ constexpr uint32_t kTileTx = kLatStage + kRopeStage;
 constexpr int kThreadsU = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                 // S^T: 2 buffers x 32 columns (token j, token j + 1)
-constexpr uint32_t kColO = 256;               // O^T: 2 buffers x 4 blocks x 32 columns (token j, token j + 1)
+constexpr uint32_t kColO = 256;               // O^T: 4 blocks x 64 columns (hi, lo x token j, j + 1), one buffer
 // Lazy max: a tile's max is taken (and O rescaled) only when a score exceeds
 // the reference max m_ref by more than kTau (log2 units). P is formed as
 // 2^(s - m_ref + kPShift) <= 2^(kTau + kPShift) = 256, inside e4m3's range
@@ -72,7 +72,7 @@ static_assert(kTau + kPShift <= 8.0f, "P must stay within e4m3's finite range");
 constexpr uint64_t kWaitLimitNsU = 2000000000ull;
 constexpr uint64_t kDrainLimitNsU = 200000000ull;
 constexpr float kLog2eU = 1.4426950408889634f;
-constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 32, 1, 1);
+constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 64, 1, 1);
 constexpr uint32_t kLayoutSw64 = 4;
 
 enum : int {
@@ -84,7 +84,7 @@ enum : int {
   kBPEmpty = 12,  // [2] P^T consumed (P.V done)
   kBQFull = 14,   // query staged (128 arrivals)
   kBQEmpty = 15,  // query consumed (last scores of the item done)
-  kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals)
+  kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals); only [0] is used: O has one buffer
   kBDrain = 18,   // every MMA of the CTA done (both issuing threads commit)
   kNumBars = 19
 };
@@ -361,20 +361,18 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const bool first = d.t0 == d.t_begin;
     // P^T of tile i sits in tile i's rope slot
     const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = rope_addr + (i & 1) * kRopeStage;
-    const uint32_t ob = tmem + kColO + 128u * (uint32_t)(d.k & 1);
+    const uint32_t ob = tmem + kColO;
     umma::fence_after_sync();
-    // B = [P_hi(j)^T | P_hi(j+1)^T], then [P_lo(j)^T | P_lo(j+1)^T] into the same
-    // columns; MN-major without swizzle: 8-token core matrices 128 B apart along K,
-    // token j+1's group kPTok after token j's along N
+    // B = [P_hi(j)^T | P_hi(j+1)^T | P_lo(j)^T | P_lo(j+1)^T], one N = 64 MMA per
+    // k-step; MN-major without swizzle: 8-token core matrices 128 B apart along K,
+    // the 16-column groups kPTok apart along N
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint64_t va = umma::smem_desc(lat + blk * kBlk + j * 4096, kBlk, 1024, umma::kLayoutSw128);
-        umma::mma_f8f6f4(ob + 32u * blk, va, umma::smem_desc(p0 + j * 512, 128, kPTok, umma::kLayoutNone), kIdescPV,
+        umma::mma_f8f6f4(ob + 64u * blk, va, umma::smem_desc(p0 + j * 512, 128, kPTok, umma::kLayoutNone), kIdescPV,
                          (first && j == 0) ? 0u : 1u);
-        umma::mma_f8f6f4(ob + 32u * blk, va, umma::smem_desc(p0 + kPLo + j * 512, 128, kPTok, umma::kLayoutNone),
-                         kIdescPV, 1u);
       }
     umma::commit(bar(kBPEmpty + (i & 1)));
     umma::commit(bar(kBREmpty + (i & 1)));
@@ -608,7 +606,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       int npv = 0;
       while (!d.done) {
         const bool first = d.t0 == d.t_begin;
-        ok = (!first || d.k < 2 || wait_u(bar(kBOEmpty + (d.k & 1)), ((d.k >> 1) - 1) & 1, abort_flag)) &&
+        ok = (!first || d.k < 1 || wait_u(bar(kBOEmpty), (d.k - 1) & 1, abort_flag)) &&
              wait_u(bar(kBPFull + (npv & 1)), (npv >> 1) & 1, abort_flag);
         if (!ok) break;
         issue_pv(d, npv);
@@ -752,20 +750,30 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             const int pt = i - 1;
             if (__all_sync(~0u, wait_u(bar(kBPEmpty + (pt & 1)), (pt >> 1) & 1, abort_flag))) {
               umma::fence_after_sync();
-              const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
+              const uint32_t ob = tmem + lane_off + kColO;
               // kept as a loop (rare path; code layout)
 #pragma unroll 1
               for (int blk = 0; blk < 4; ++blk) {
                 float o0[16], o1[16];
-                umma::tmem_ld16(ob + 32u * blk, o0);
-                umma::tmem_ld16(ob + 32u * blk + 16u, o1);
+                umma::tmem_ld16(ob + 64u * blk, o0);
+                umma::tmem_ld16(ob + 64u * blk + 16u, o1);
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                   o0[h] *= al0[h];
                   o1[h] *= al1[h];
                 }
-                umma::tmem_st16(ob + 32u * blk, o0);
-                umma::tmem_st16(ob + 32u * blk + 16u, o1);
+                umma::tmem_st16(ob + 64u * blk, o0);
+                umma::tmem_st16(ob + 64u * blk + 16u, o1);
+                // the lo columns of both tokens
+                umma::tmem_ld16(ob + 64u * blk + 32u, o0);
+                umma::tmem_ld16(ob + 64u * blk + 48u, o1);
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                  o0[h] *= al0[h];
+                  o1[h] *= al1[h];
+                }
+                umma::tmem_st16(ob + 64u * blk + 32u, o0);
+                umma::tmem_st16(ob + 64u * blk + 48u, o1);
               }
               umma::tmem_wait_st();
             } else {
@@ -840,7 +848,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       }
       (void)ptx::named_bar_or(1, 128, false);
       umma::fence_after_sync();
-      const uint32_t ob = tmem + lane_off + kColO + 128u * (uint32_t)(k & 1);
+      const uint32_t ob = tmem + lane_off + kColO;
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {  // token j, then token j + 1
         float inv[16];
@@ -853,7 +861,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
           float o[16];
-          umma::tmem_ld16(ob + 32u * blk + 16u * t, o);
+          float o_lo[16];
+          umma::tmem_ld16(ob + 64u * blk + 16u * t, o);
+          umma::tmem_ld16(ob + 64u * blk + 32u + 16u * t, o_lo);
+#pragma unroll
+          for (int h = 0; h < 16; ++h) o[h] += o_lo[h];
           const int dcol = 128 * blk + row;
           if (w.slot < 0) {
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)(w.q_row + t) * kHeads * kVDim + dcol;
@@ -879,7 +891,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
       }
       umma::fence_before_sync();
-      umma::mbar_arrive(bar(kBOEmpty + (k & 1)));
+      umma::mbar_arrive(bar(kBOEmpty));
       ++k;
     }
     if (aborted && tid == 0) record_error_u(p.err, MLA_ERR_TIMEOUT);
