@@ -485,7 +485,8 @@ def bench_ours(args):
         "config": {"workload": args.workload, "desc": w.describe(), "batch": w.batch, "kv_rows": nbytes["rows"],
                    "heads": 16, "qk_dim": 576, "v_dim": 512, "page_size": page_size,
                    "kv_order": "shuffled" if shuffled else ("workload" if kind == "rows" else "in order"),
-                   "q_len": q_len, "causal": q_len > 1, "token_pairs": bool(plan.token_pairs),
+                   "q_len": q_len, "causal": q_len > 1,
+                   "token_pairs": bool(plan.token_pairs) and w.mode == mi.MODE_FP8 and args.fp8_kernel == 0,
                    "bytes_per_call": step_bytes,
                    "l2": (f"{n_copies} input copies rotate call after call "
                           + ("(each larger than L2)" if n_copies == 2 and step_bytes > l2_bytes(dev)
@@ -651,8 +652,9 @@ def main():
     ap.add_argument("--layout", default="rows",
                     help="KV layout of the workload: rows (its own order), rows:shuffled, pages:N, pages:N:shuffled")
     ap.add_argument("--q-len", type=int, default=1, help="query tokens per sequence (causal)")
-    ap.add_argument("--token-pairs", type=int, default=0, choices=[0, 1],
-                    help="several query tokens, fp8: plan tokens in pairs, one pass over the rows per pair")
+    ap.add_argument("--token-pairs", type=int, default=0, choices=[-1, 0, 1],
+                    help="several query tokens, fp8 tensor-core kernel: two tokens per pass over the rows "
+                         "(0 default: on, -1: one CTA per token)")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

@@ -110,14 +110,14 @@ typedef struct mla_plan_options {
                              token and give each range Q CTAs, one per token, which read the same rows
                              at the same time (from HBM once, from L2 for the others). 0 = default (on);
                              negative = off: each range's tokens run back to back in one CTA. */
-  int token_pairs;        /* several query tokens, fp8 only: when every sequence with KV rows has the same
-                             even number Q of query tokens, take tokens 2v and 2v+1 of a sequence in one
-                             pass over their rows (both queries in one 32-column score MMA), which reads
-                             each KV tile once for two tokens. token_parallel then applies to the Q/2
-                             pairs. > 0 = on; 0 = default (off). A plan made with pairs serves only
-                             mla_decode_multi with dtype_mode MLA_MODE_FP8 on the tensor-core kernel
-                             (fp8_kernel 0); other modes return MLA_ERR_ARG. Without an even, equal Q
-                             the plan is the ordinary one. */
+  int token_pairs;        /* several query tokens (mla_decode_plan_multi): when every sequence with KV rows
+                             has the same even number Q of query tokens, the plan also holds a work list
+                             in token pairs: tokens 2v and 2v+1 of a sequence in one pass over their
+                             rows (both queries in one 32-column score MMA), which reads each KV tile
+                             once for two tokens; token_parallel then applies to the Q/2 pairs.
+                             mla_decode_multi uses it for MLA_MODE_FP8 on the tensor-core kernel
+                             (fp8_kernel 0), and the ordinary list for every other decode. 0 = default
+                             (on); negative = off; positive = on. */
 } mla_plan_options;
 
 /* Read-only description of a plan. */
@@ -131,7 +131,8 @@ typedef struct mla_plan_info {
   int64_t total_rows;     /* sum of the sequence lengths */
   int64_t max_rows_per_cta;
   size_t workspace_bytes; /* device bytes the plan owns */
-  int token_pairs;        /* 1: the work items are token pairs (option token_pairs took effect) */
+  int token_pairs;        /* 1: the plan also holds a token-pair work list (the other fields describe the
+                             ordinary list) */
 } mla_plan_info;
 
 /*

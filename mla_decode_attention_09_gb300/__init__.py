@@ -188,7 +188,7 @@ class Plan:
 
     @property
     def token_pairs(self) -> bool:
-        """The plan's items are token pairs (served by the fp8 tensor-core pair kernel only)."""
+        """The plan also holds a token-pair work list (used by fp8 decodes on the tensor-core kernel)."""
         return bool(self.info()["token_pairs"])
 
     def info(self) -> dict:

@@ -2,6 +2,7 @@
 // validation, and the stage-1 / reduce launches. No exception leaves this file.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -25,6 +26,13 @@ struct mla_plan {
   std::vector<int32_t> qo_indptr;
   mla::HostPlan host;
   mla::DevicePlan dev{};
+  // Several query tokens: a second work list in token pairs, built unless the option turns it
+  // off and only when the query counts allow it; fp8 decodes on the tensor-core kernel use it,
+  // every other decode the first list. Both share the partial buffers and the error word.
+  bool want_pairs = false;
+  bool has_pairs = false;
+  mla::HostPlan host_pairs;
+  mla::DevicePlan dev_pairs{};
   void* block = nullptr;         // single device allocation backing every buffer
   size_t block_bytes = 0;
   const void* zero_row = nullptr;  // 1152 zero bytes (source for tail rows of a tile)
@@ -57,13 +65,13 @@ bool same_array(const std::vector<int32_t>& v, const int32_t* a, size_t n) {
 }
 
 bool same_key(const mla_plan* p, int device, int batch, const int32_t* indptr, const Layout& l, int num_sms,
-              const mla::PlanOptions& o) {
+              const mla::PlanOptions& o, bool want_pairs) {
   return p->device == device && p->batch == batch && p->num_sms == num_sms && p->kind == l.kind &&
          p->page_size == l.page_size && p->causal == l.causal && p->opt.num_kv_slots == o.num_kv_slots &&
          p->opt.min_rows_per_split == o.min_rows_per_split && p->opt.granularity == o.granularity &&
          p->opt.ctas_per_sm == o.ctas_per_sm && p->opt.fp8_kernel == o.fp8_kernel &&
          p->opt.fp8_issuers == o.fp8_issuers && p->opt.item_cost_rows == o.item_cost_rows &&
-         p->opt.token_parallel == o.token_parallel && p->opt.token_pairs == o.token_pairs &&
+         p->opt.token_parallel == o.token_parallel && p->want_pairs == want_pairs &&
          std::memcmp(p->indptr.data(), indptr, sizeof(int32_t) * (size_t)(batch + 1)) == 0 &&
          same_array(p->last_page_len, l.last, (size_t)batch) &&
          same_array(p->qo_indptr, l.qo, batch > 0 ? (size_t)batch + 1 : 0);
@@ -78,6 +86,7 @@ void destroy_plan(mla_plan* p) {
     if (cur != p->device && cur >= 0) cudaSetDevice(cur);
   }
   mla::free_host_plan(&p->host);
+  mla::free_host_plan(&p->host_pairs);
   delete p;
 }
 
@@ -94,7 +103,7 @@ int check_device(int* device_out) {
 }
 
 int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num_sms, const mla::PlanOptions& opt,
-              int device, mla_plan** out) {
+              bool want_pairs, int device, mla_plan** out) {
   mla_plan* p = new (std::nothrow) mla_plan();
   if (!p) return MLA_ERR_NOMEM;
   p->device = device;
@@ -107,17 +116,30 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   p->indptr.assign(kv_indptr_host, kv_indptr_host + batch + 1);
   if (l.last && batch > 0) p->last_page_len.assign(l.last, l.last + batch);
   if (l.qo && batch > 0) p->qo_indptr.assign(l.qo, l.qo + batch + 1);
+  p->want_pairs = want_pairs;
+  mla::PlanOptions opt_main = opt;
+  opt_main.token_pairs = false;
   int rc = l.kind == kMultiKind
-               ? mla::build_host_plan_multi(batch, l.qo, kv_indptr_host, l.last, l.page_size, l.causal, num_sms, opt,
-                                            &p->host)
-           : l.kind == kPagedKind ? mla::build_host_plan_paged(batch, kv_indptr_host, l.last, l.page_size, num_sms, opt,
-                                                               &p->host)
-                                  : mla::build_host_plan(batch, kv_indptr_host, num_sms, opt, &p->host);
+               ? mla::build_host_plan_multi(batch, l.qo, kv_indptr_host, l.last, l.page_size, l.causal, num_sms,
+                                            opt_main, &p->host)
+           : l.kind == kPagedKind ? mla::build_host_plan_paged(batch, kv_indptr_host, l.last, l.page_size, num_sms,
+                                                               opt_main, &p->host)
+                                  : mla::build_host_plan(batch, kv_indptr_host, num_sms, opt_main, &p->host);
+  if (rc == MLA_OK && l.kind == kMultiKind && want_pairs) {
+    mla::PlanOptions opt_pairs = opt;
+    opt_pairs.token_pairs = true;
+    rc = mla::build_host_plan_multi(batch, l.qo, kv_indptr_host, l.last, l.page_size, l.causal, num_sms, opt_pairs,
+                                    &p->host_pairs);
+    p->has_pairs = rc == MLA_OK && p->host_pairs.token_pairs;
+    if (rc == MLA_OK && !p->has_pairs) mla::free_host_plan(&p->host_pairs);  // the counts do not pair up
+  }
   if (rc != MLA_OK) {
-    delete p;
+    destroy_plan(p);
     return rc;
   }
   const mla::HostPlan& h = p->host;
+  const mla::HostPlan& hp = p->host_pairs;
+  const int slots = p->has_pairs ? std::max(h.num_slots, hp.num_slots) : h.num_slots;
   // layout of the single device block
   size_t off = 0;
   const size_t o_items = off;
@@ -126,10 +148,16 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   off = align_up(off + sizeof(int32_t) * (size_t)(h.num_ctas + 1), 256);
   const size_t o_reduce = off;
   off = align_up(off + sizeof(mla::ReduceEntry) * (size_t)h.n_reduce, 256);
+  const size_t o_items_p = off;
+  if (p->has_pairs) off = align_up(off + sizeof(mla::WorkItem) * (size_t)hp.n_items, 256);
+  const size_t o_indptr_p = off;
+  if (p->has_pairs) off = align_up(off + sizeof(int32_t) * (size_t)(hp.num_ctas + 1), 256);
+  const size_t o_reduce_p = off;
+  if (p->has_pairs) off = align_up(off + sizeof(mla::ReduceEntry) * (size_t)hp.n_reduce, 256);
   const size_t o_po = off;
-  off = align_up(off + sizeof(float) * (size_t)h.num_slots * mla::kHeads * mla::kVDim, 256);
+  off = align_up(off + sizeof(float) * (size_t)slots * mla::kHeads * mla::kVDim, 256);
   const size_t o_lse = off;
-  off = align_up(off + sizeof(float) * (size_t)h.num_slots * mla::kHeads, 256);
+  off = align_up(off + sizeof(float) * (size_t)slots * mla::kHeads, 256);
   const size_t o_err = off;
   off = align_up(off + sizeof(int), 256);
   const size_t o_zero = off;
@@ -142,10 +170,16 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
     return MLA_ERR_NOMEM;
   }
   char* base = static_cast<char*>(p->block);
-  std::vector<char> staging(o_po, 0);  // items, indptr and reduce map, uploaded in one copy
+  std::vector<char> staging(o_po, 0);  // work lists and reduce maps, uploaded in one copy
   if (h.n_items) std::memcpy(staging.data() + o_items, h.items, sizeof(mla::WorkItem) * (size_t)h.n_items);
   std::memcpy(staging.data() + o_indptr, h.work_indptr, sizeof(int32_t) * (size_t)(h.num_ctas + 1));
   if (h.n_reduce) std::memcpy(staging.data() + o_reduce, h.reduce, sizeof(mla::ReduceEntry) * (size_t)h.n_reduce);
+  if (p->has_pairs) {
+    if (hp.n_items) std::memcpy(staging.data() + o_items_p, hp.items, sizeof(mla::WorkItem) * (size_t)hp.n_items);
+    std::memcpy(staging.data() + o_indptr_p, hp.work_indptr, sizeof(int32_t) * (size_t)(hp.num_ctas + 1));
+    if (hp.n_reduce)
+      std::memcpy(staging.data() + o_reduce_p, hp.reduce, sizeof(mla::ReduceEntry) * (size_t)hp.n_reduce);
+  }
   if (cudaMemcpy(base, staging.data(), o_po, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemset(base + o_err, 0, off - o_err) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
@@ -165,7 +199,19 @@ int make_plan(int batch, const int32_t* kv_indptr_host, const Layout& l, int num
   for (int i = 0; i < h.n_reduce; ++i) p->dev.reduce_max_slots = std::max(p->dev.reduce_max_slots, h.reduce[i].n_slots);
   p->dev.fp8_kernel = opt.fp8_kernel;
   p->dev.dual_issue = mla::dual_issue(opt) ? 1 : 0;
-  p->dev.token_pairs = h.token_pairs ? 1 : 0;
+  p->dev.token_pairs = 0;
+  if (p->has_pairs) {
+    p->dev_pairs = p->dev;
+    p->dev_pairs.items = reinterpret_cast<const mla::WorkItem*>(base + o_items_p);
+    p->dev_pairs.work_indptr = reinterpret_cast<const int32_t*>(base + o_indptr_p);
+    p->dev_pairs.reduce = reinterpret_cast<const mla::ReduceEntry*>(base + o_reduce_p);
+    p->dev_pairs.num_ctas = hp.num_ctas;
+    p->dev_pairs.n_reduce = hp.n_reduce;
+    p->dev_pairs.reduce_max_slots = 0;
+    for (int i = 0; i < hp.n_reduce; ++i)
+      p->dev_pairs.reduce_max_slots = std::max(p->dev_pairs.reduce_max_slots, hp.reduce[i].n_slots);
+    p->dev_pairs.token_pairs = 1;
+  }
   p->zero_row = base + o_zero;
   p->refcount = 1;
   *out = p;
@@ -181,8 +227,6 @@ int validate_decode(const void* q, const void* kv, const float* kv_scale, const 
   if (l.kind == kMultiKind && plan->batch > 0 && !l.qo) return MLA_ERR_ARG;
   if (dtype_mode != MLA_MODE_BF16 && dtype_mode != MLA_MODE_FP8 && dtype_mode != MLA_MODE_A16W8)
     return MLA_ERR_DTYPE;
-  // token-pair items are understood by the fp8 tensor-core pair kernel only
-  if (plan->dev.token_pairs && (dtype_mode != MLA_MODE_FP8 || plan->dev.fp8_kernel != 0)) return MLA_ERR_ARG;
   if (plan->batch > 0) {
     if (!q || !kv || !kv_indptr || !out) return MLA_ERR_ARG;
     if (plan->host.total_rows > 0 && !kv_indices) return MLA_ERR_ARG;
@@ -210,18 +254,20 @@ int plan_common(int batch, const int32_t* kv_indptr_host, const Layout& layout, 
         return MLA_ERR_CUDA;
     }
     const mla::PlanOptions opt = mla::resolve_options(options);
+    // the token-pair list of a multi-token plan: on unless the option is negative
+    const bool want_pairs = layout.kind == kMultiKind && !(options && options->token_pairs < 0);
     static const int32_t kZero = 0;
     const int32_t* indptr = batch > 0 ? kv_indptr_host : &kZero;
     std::lock_guard<std::mutex> lock(g_mu);
     for (mla_plan* p : g_cache) {
-      if (same_key(p, device, batch, indptr, layout, num_sms, opt)) {
+      if (same_key(p, device, batch, indptr, layout, num_sms, opt, want_pairs)) {
         ++p->refcount;
         *plan_out = p;
         return MLA_OK;
       }
     }
     mla_plan* p = nullptr;
-    rc = make_plan(batch, indptr, layout, num_sms, opt, device, &p);
+    rc = make_plan(batch, indptr, layout, num_sms, opt, want_pairs, device, &p);
     if (rc != MLA_OK) return rc;
     g_cache.push_back(p);
     *plan_out = p;
@@ -233,12 +279,15 @@ int plan_common(int batch, const int32_t* kv_indptr_host, const Layout& layout, 
 
 int decode_common(const mla::DecodeArgs& a, int dtype_mode, mla_plan* workspace, void* stream, bool reduce) {
   if (workspace->batch == 0) return MLA_OK;
-  const int rc = workspace->dev.token_pairs ? mla::launch_stage1_fp8_pairs_umma(a, workspace->dev, stream)
-                                            : mla::launch_stage1(dtype_mode, a, workspace->dev, workspace->zero_row, stream);
+  // fp8 on the tensor-core kernel takes the token-pair list when the plan has one
+  const bool pairs = workspace->has_pairs && dtype_mode == MLA_MODE_FP8 && workspace->dev.fp8_kernel == 0;
+  const mla::DevicePlan& dv = pairs ? workspace->dev_pairs : workspace->dev;
+  const int rc = pairs ? mla::launch_stage1_fp8_pairs_umma(a, dv, stream)
+                       : mla::launch_stage1(dtype_mode, a, dv, workspace->zero_row, stream);
   if (rc != 0) return MLA_ERR_CUDA;
   // the reduce is launched programmatically dependent: it starts while stage 1
   // drains and waits for its results on the device
-  if (reduce && mla::launch_reduce(a.out, workspace->dev, stream, true) != 0) return MLA_ERR_CUDA;
+  if (reduce && mla::launch_reduce(a.out, dv, stream, true) != 0) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -301,7 +350,7 @@ int mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   info->total_rows = plan->host.total_rows;
   info->max_rows_per_cta = plan->host.max_rows_per_cta;
   info->workspace_bytes = plan->block_bytes;
-  info->token_pairs = plan->dev.token_pairs;
+  info->token_pairs = plan->has_pairs ? 1 : 0;
   return MLA_OK;
 }
 

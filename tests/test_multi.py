@@ -107,8 +107,10 @@ def test_multi_query_mismatch_is_reported(mla):
     assert e.value.status == -1
 
 
-# Speculative-decode shape: fp8, B = 64, kv_len = 8192, two query tokens per sequence.
-@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
+# Speculative-decode shape: fp8, B = 64, kv_len = 8192, two query tokens per sequence. On the
+# tensor-core kernel the default plan takes the tokens in pairs; token_pairs = -1 keeps one CTA
+# per token.
+@pytest.mark.parametrize("k8", FP8_KERNELS + [{"token_pairs": -1}], ids=FP8_KERNEL_IDS + ["tcgen05-per-token"])
 def test_multi_full_size(mla, k8):
     inp = mi.make_workload("fp8_b64_l8192")
     q, qo = mi.make_query_tokens([2] * 64, seed=91)
@@ -119,8 +121,9 @@ def test_multi_full_size(mla, k8):
 
 
 # ---------------------------------------------------------------- token pairs (fp8, tensor cores)
-# Plans made with token_pairs = 1 take query tokens 2v and 2v+1 of a sequence in one pass over
-# their rows (mla_decode_attention_09_gb300/csrc/stage1_umma_pairs.cu).
+# Multi-token plans with equal even query counts also hold a token-pair list (option token_pairs,
+# on by default): fp8 on the tensor-core kernel takes tokens 2v and 2v+1 of a sequence in one pass
+# over their rows (mla_decode_attention_09_gb300/csrc/stage1_umma_pairs.cu).
 PAIRS = {"token_pairs": 1}
 
 
@@ -183,17 +186,31 @@ def test_token_pairs_edge_items(mla):
     compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, "token pairs edge items")
 
 
-def test_token_pairs_need_the_fp8_tensor_core_kernel(mla):
-    inp = mi.make_inputs([300, 40], mi.MODE_BF16, seed=450)
-    q, qo = mi.make_query_tokens([2, 2], seed=451)
-    d = inp.to("cuda")
-    out = torch.zeros((4, 16, 512), dtype=torch.bfloat16, device="cuda")
-    for mode, extra in ((mi.MODE_BF16, {}), (mi.MODE_A16W8, {}), (mi.MODE_FP8, {"fp8_kernel": 1})):
-        plan = mla.plan_multi(qo, inp.kv_indptr, causal=True, **PAIRS, **extra)
-        with pytest.raises(mla.MLAError) as e:
-            mla.decode_multi(q.cuda(), d.kv, torch.ones(1, device="cuda"), qo.cuda(), d.kv_indptr, d.kv_indices, out,
-                             plan=plan, dtype_mode=mode)
-        assert e.value.status == -1
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+def test_token_pair_plans_serve_every_mode(mla, mode, k8):
+    # a plan with a token-pair list (the default for equal even counts): fp8 on the tensor-core
+    # kernel takes the pairs, every other mode and kernel the ordinary list
+    inp = mi.make_inputs([300, 40, 1000, 2], mode, seed=450 + mode, permute=True, extra_slots=5)
+    q, qo = mi.make_query_tokens([2, 2, 2, 2], seed=451, q_std=2.0)
+    out, plan = run_multi(mla, inp, q, qo, True, num_sms=12, min_rows_per_split=16, granularity=16, **k8)
+    assert plan.token_pairs and plan.check_error() == 0
+    compare(out, oracle_multi(inp, q, qo, True), mode, f"token-pair plan, mode {mode}")
+
+
+@pytest.mark.parametrize("qn", [2, 4])
+@pytest.mark.parametrize("split", ["whole", "split"])
+@pytest.mark.parametrize("layout", ["rows", "pages64"])
+def test_multi_tokens_equal_counts_per_token_ctas(mla, qn, split, layout):
+    # fp8 on the tensor-core kernel with the token-pair list turned off: one CTA per token
+    lengths = [1, 130, 640, 1000, 3 * 128 + 5, 7 * 128, 2000]
+    mode = mi.MODE_FP8
+    inp = (mi.make_paged_inputs(lengths, 64, mode, seed=460 + qn, permute=True, extra_pages=3)
+           if layout == "pages64" else mi.make_inputs(lengths, mode, seed=460 + qn, permute=True, extra_slots=7))
+    q, qo = mi.make_query_tokens([qn] * len(lengths), seed=470 + qn, q_std=2.0)
+    opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
+    out, plan = run_multi(mla, inp, q, qo, True, num_sms=152 if split == "whole" else 12, token_pairs=-1, **opts)
+    assert not plan.token_pairs and plan.check_error() == 0
+    compare(out, oracle_multi(inp, q, qo, True), mode, f"per-token CTAs q={qn} {split}")
 
 
 @pytest.mark.parametrize("qn", [2, 4])
