@@ -136,7 +136,7 @@ def pair_items(mla, qo, inp, num_sms, causal, **opts):
 @pytest.mark.parametrize("qn", [2, 4])
 @pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
 @pytest.mark.parametrize("split", ["whole", "split"])
-@pytest.mark.parametrize("layout", ["rows", "pages64", "pages8"])
+@pytest.mark.parametrize("layout", ["rows", "pages64", "pages8", "pages3"])
 def test_token_pairs(mla, qn, causal, split, layout):
     lengths = [1, 2, 3, 130, 640, 1000, 3 * 128 + 5, 7 * 128, 2000, 65]
     mode = mi.MODE_FP8
@@ -144,8 +144,7 @@ def test_token_pairs(mla, qn, causal, split, layout):
     if layout == "rows":
         inp = mi.make_inputs(lengths, mode, seed=seed, permute=True, extra_slots=7)
     else:
-        inp = mi.make_paged_inputs(lengths, 64 if layout == "pages64" else 8, mode, seed=seed, permute=True,
-                                   extra_pages=3)
+        inp = mi.make_paged_inputs(lengths, int(layout[5:]), mode, seed=seed, permute=True, extra_pages=3)
     q, qo = mi.make_query_tokens([qn] * len(lengths), seed=seed + 1, q_std=2.0)
     opts = {} if split == "whole" else {"min_rows_per_split": 16, "granularity": 16}
     num_sms = 152 if split == "whole" else 12
