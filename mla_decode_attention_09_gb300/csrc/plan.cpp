@@ -94,7 +94,8 @@ int plan_tokens(int batch, const std::vector<int64_t>& tok, const std::vector<in
   // and from L2 for the other tokens (a range processing its tokens back to back
   // re-reads them from HBM once the ranges outgrow L2).
   //
-  // Token pairs (opt-in): when that Q is even, query tokens 2v and 2v+1 of a
+  // Token pairs (asked for by the option; a multi-token plan builds this list
+  // beside the per-token one): when that Q is even, query tokens 2v and 2v+1 of a
   // sequence form one unit, processed in one pass over their rows by the fp8
   // tensor-core kernel. A pair item covers rows [t_begin, t_end) for token
   // 2v+1 and [t_begin, pad) for token 2v (pad >= t_begin), and its two partial
