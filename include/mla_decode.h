@@ -361,7 +361,9 @@ int mla_plan_compute_host_paged(int batch, const int32_t* kv_indptr_host, const 
  * side: they read each row at about the same time, from HBM once and from L2
  * for the other tokens (option token_parallel). Otherwise one CTA processes the
  * query tokens of a range back to back on the same rows, which find them in L2
- * only while the CTAs' ranges fit in it.
+ * only while the CTAs' ranges fit in it. When that number Q is even, the plan
+ * also holds a work list in token pairs, which fp8 decodes on the tensor-core
+ * kernel use: two tokens per pass over their rows (option token_pairs).
  *
  * mla_decode_plan_multi — the planner for that layout (host arrays as for
  *   mla_decode_plan_paged, plus qo_indptr_host [B+1], 0 first, non-decreasing).
