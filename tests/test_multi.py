@@ -219,3 +219,29 @@ def test_token_pairs_full_size(mla, qn):
     out, plan = run_multi(mla, inp, q, qo, True, **PAIRS)
     assert plan.check_error() == 0
     compare(out, oracle_multi(inp, q, qo, True), mi.MODE_FP8, f"token pairs full size q={qn}")
+
+
+def test_token_pairs_out_of_range_index_is_reported(mla):
+    inp = mi.make_inputs([300, 200], mi.MODE_FP8, seed=4)
+    inp.kv_indices[7] = inp.kv.shape[0] + 5
+    q, qo = mi.make_query_tokens([2, 2], seed=5)
+    out, plan = run_multi(mla, inp, q, qo, True)
+    assert plan.token_pairs
+    assert plan.check_error() == -8   # MLA_ERR_INDEX; the bad row was read as zeros
+    assert torch.isfinite(out.float()).all()
+
+
+def test_token_pairs_query_mismatch_is_reported(mla):
+    # the device qo_indptr disagrees with the plan: the pair kernel checks both rows of a pair and
+    # skips the items instead of reading another sequence's query
+    inp = mi.make_inputs([64, 40], mi.MODE_FP8, seed=8)
+    q, qo = mi.make_query_tokens([2, 2], seed=9)
+    d = inp.to("cuda")
+    plan = mla.plan_multi(qo, inp.kv_indptr, num_kv_slots=inp.kv.shape[0])
+    assert plan.token_pairs
+    bad = torch.tensor([0, 1, 4], dtype=torch.int32, device="cuda")
+    out = torch.zeros((4, 16, 512), dtype=torch.bfloat16, device="cuda")
+    mla.decode_multi(q.cuda(), d.kv, d.kv_scale_tensor("cuda"), bad, d.kv_indptr, d.kv_indices, out, plan=plan,
+                     dtype_mode=mi.MODE_FP8)
+    assert plan.check_error() == -3   # MLA_ERR_PLAN_MISMATCH
+    assert not out.float().abs().any()  # nothing was written

@@ -219,14 +219,15 @@ def test_plan_mismatch_is_reported(mla):
     assert plan.check_error() == 0    # cleared after reading
 
 
-@pytest.mark.parametrize("k8", FP8_KERNELS, ids=FP8_KERNEL_IDS)
-def test_out_of_range_index_is_reported(mla, k8):
-    inp = mi.make_inputs([30, 20], mi.MODE_FP8, seed=4)
+@pytest.mark.parametrize("mode,k8", [(mi.MODE_FP8, k) for k in FP8_KERNELS] + [(mi.MODE_A16W8, {})],
+                         ids=[f"fp8-{k}" for k in FP8_KERNEL_IDS] + ["a16w8-tcgen05"])
+def test_out_of_range_index_is_reported(mla, mode, k8):
+    inp = mi.make_inputs([30, 20], mode, seed=4)
     inp.kv_indices[7] = inp.kv.shape[0] + 5
     d = inp.to("cuda")
     plan = mla.plan(inp.kv_indptr, 0, num_kv_slots=inp.kv.shape[0], **k8)
     out = torch.zeros((2, 16, 512), dtype=torch.bfloat16, device="cuda")
-    mla.decode(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, out, plan=plan)
+    mla.decode(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, out, plan=plan, dtype_mode=mode)
     assert plan.check_error() == -8   # MLA_ERR_INDEX; the bad row was read as zeros
     assert torch.isfinite(out.float()).all()
 
