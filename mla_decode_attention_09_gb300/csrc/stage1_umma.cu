@@ -37,8 +37,9 @@
 // (512 B per row, needed until P.V finishes) lives in a 3-slot ring of 64 KB,
 // the rope part (64 B per row, needed only by the scores) in a 2-slot ring of
 // 8 KB, so three tiles can be resident or in flight. S, P and O are double
-// buffered. The producer and the single MMA thread poll their barriers and
-// never block one activity on another. The running max per head is updated lazily:
+// buffered. The main loader polls its barriers, since it also stages queries;
+// the lone MMA thread of the one-issuer instance polls both of its chains; the
+// two issuers of kDual wait on theirs. The running max per head is updated lazily:
 // O in TMEM is rescaled only when a tile's max exceeds the reference by more
 // than 2^3, so P = 2^(s - m_ref + 5) <= 256 stays inside e4m3's range.
 //
