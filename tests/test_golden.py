@@ -9,7 +9,10 @@ closed_forms.txt holds one-sequence cases with constant rows and a constant quer
 output O is worked out by hand in the file. The oracle must reproduce O in float64 on the
 CPU; every stage-1 kernel must produce its bf16 rounding exactly, both on the sequence as
 written and with its rows repeated until the plan splits it (repeating every row k times
-multiplies the softmax's numerator and denominator by k, so O is unchanged).
+multiplies the softmax's numerator and denominator by k, so O is unchanged). The same
+values hold in every KV layout (rows spread over pages in any order, the unused rows of
+the last page poisoned), and for every query token of a sequence when each token sees
+all of its rows (several tokens, not causal), so those paths are checked against them too.
 """
 import os
 import re
@@ -65,6 +68,29 @@ def make_case(a: float, rows, mode: int, repeat: int = 1) -> mi.Inputs:
     codes = kv.to(torch.float8_e4m3fn)
     assert torch.equal(codes.float(), kv)  # the fixtures' values are exact in e4m3
     return mi.Inputs(mode, q, codes.view(torch.uint8).contiguous(), 1.0, ip, ix, sm_scale=mi.SM_SCALE)
+
+
+POISON = 448.0  # the unused rows of a last page: exact in bf16 and e4m3, and far from every case's rows
+
+
+def make_paged_case(a: float, rows, mode: int, repeat: int, page_size: int, seed: int = 7) -> mi.Inputs:
+    """make_case's rows laid out in pages of page_size, in a shuffled page order, with the
+    unused rows of the last page holding POISON."""
+    base = make_case(a, rows, mode, repeat)
+    n = base.kv.shape[0]
+    pages = -(-n // page_size)
+    perm = torch.randperm(pages, generator=torch.Generator().manual_seed(seed))
+    fill = torch.full((1, mi.QK_DIM), POISON)
+    fill = fill.to(torch.bfloat16) if mode == mi.MODE_BF16 else fill.to(torch.float8_e4m3fn).view(torch.uint8)
+    buf = fill.expand(pages * page_size, -1).clone()
+    for p_log in range(pages):
+        lo, hi = p_log * page_size, min((p_log + 1) * page_size, n)
+        dst = int(perm[p_log]) * page_size
+        buf[dst:dst + hi - lo] = base.kv[lo:hi]
+    ip = torch.tensor([0, pages], dtype=torch.int32)
+    last = torch.tensor([n - (pages - 1) * page_size], dtype=torch.int32)
+    return mi.Inputs(mode, base.q, buf.contiguous(), 1.0, ip, perm.to(torch.int32), sm_scale=mi.SM_SCALE,
+                     page_size=page_size, kv_last_page_len=last)
 
 
 # ---------------------------------------------------------------- printed constants
@@ -160,6 +186,49 @@ def test_closed_forms_gpu(mla, case, kernel, repeat):
     out = torch.empty((1, mi.HEADS, mi.V_DIM), dtype=torch.bfloat16, device="cuda")
     mla.decode(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, out, plan=plan,
                sm_scale=d.sm_scale, dtype_mode=mode)
+    assert plan.check_error() == 0
+    got = out.float().cpu()
+    assert torch.equal(got, torch.full_like(got, expect_bf16)), (name, got.min().item(), got.max().item())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("page_size", [3, 8, 16, 64], ids=lambda p: f"pages{p}")
+@pytest.mark.parametrize("kernel", KERNELS, ids=[k[0] for k in KERNELS])
+@pytest.mark.parametrize("case", CASES, ids=CASE_IDS)
+def test_closed_forms_gpu_paged(mla, case, kernel, page_size):
+    """Pages in shuffled order, the last page's unused rows poisoned; split over CTAs."""
+    name, a, rows, _, expect_bf16 = case
+    _, mode, opts = kernel
+    inp = make_paged_case(a, rows, mode, 500, page_size)
+    d = inp.to("cuda")
+    plan = mla.plan_paged(inp.kv_indptr, inp.kv_last_page_len, page_size, num_kv_slots=inp.kv.shape[0], **opts)
+    out = torch.empty((1, mi.HEADS, mi.V_DIM), dtype=torch.bfloat16, device="cuda")
+    mla.decode_paged(d.q, d.kv, d.kv_scale_tensor("cuda"), d.kv_indptr, d.kv_indices, d.kv_last_page_len, page_size,
+                     out, plan=plan, sm_scale=d.sm_scale, dtype_mode=mode)
+    assert plan.check_error() == 0
+    got = out.float().cpu()
+    assert torch.equal(got, torch.full_like(got, expect_bf16)), (name, got.min().item(), got.max().item())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("q_len", [2, 3, 4])
+@pytest.mark.parametrize("kernel", KERNELS, ids=[k[0] for k in KERNELS])
+@pytest.mark.parametrize("case", CASES, ids=CASE_IDS)
+def test_closed_forms_gpu_multi(mla, case, kernel, q_len):
+    """q_len tokens that each see every row (not causal): every token's output is O. With an
+    even q_len, fp8 on the tensor cores takes the tokens in pairs."""
+    name, a, rows, _, expect_bf16 = case
+    _, mode, opts = kernel
+    inp = make_case(a, rows, mode, 500)
+    q = inp.q.expand(q_len, -1, -1).contiguous()
+    qo = torch.tensor([0, q_len], dtype=torch.int32)
+    d = inp.to("cuda")
+    plan = mla.plan_multi(qo, inp.kv_indptr, causal=False, num_kv_slots=inp.kv.shape[0], **opts)
+    if mode == mi.MODE_FP8 and "fp8_kernel" not in opts:
+        assert plan.token_pairs == (q_len % 2 == 0)
+    out = torch.empty((q_len, mi.HEADS, mi.V_DIM), dtype=torch.bfloat16, device="cuda")
+    mla.decode_multi(q.cuda(), d.kv, d.kv_scale_tensor("cuda"), qo.cuda(), d.kv_indptr, d.kv_indices, out, plan=plan,
+                     sm_scale=d.sm_scale, dtype_mode=mode)
     assert plan.check_error() == 0
     got = out.float().cpu()
     assert torch.equal(got, torch.full_like(got, expect_bf16)), (name, got.min().item(), got.max().item())
