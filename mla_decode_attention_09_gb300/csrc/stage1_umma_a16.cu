@@ -15,10 +15,18 @@
 // the lazy running max, the epilogue and the bounded waits.
 //
 // What differs from the fp8 kernel:
-// - The staged query is 18 KB. To fit, a tile's P lives in that tile's rope
-//   slot: the rope bytes are dead once the tile's scores are done, and the slot
-//   takes the next rope part once the tile's P.V is done. The two rope slots
-//   are then the two P buffers, and no shared memory is spent on P.
+// - The staged query is 18 KB. To fit, a tile's P (4 KB) lives where the tile's
+//   rope bytes were, dead once its scores are done; no other shared memory is
+//   spent on P. The 16 KB of rope space is laid out per instance:
+//   - Paged instance: two 8 KB rope slots. A slot takes the next rope part once
+//     the P.V of its tile (whose P it holds) is done, so two tiles are in flight.
+//   - Row instance: the rope part as two 32-byte halves per row (4 KB each,
+//     32-byte swizzle). Three A blocks go with the three latent slots: block A of
+//     a slot takes the tile's first half together with its latent part, then the
+//     tile's P, and frees with the slot when the tile's P.V is done. One B block
+//     takes the second half of one tile at a time, as soon as the scores of the
+//     tile before are done. Only the second half then waits on a chain that short;
+//     the P of a tile holds no slot the next tiles' rope parts need.
 // - The shared memory then holds 68 bytes less than the slack the fp8 kernel
 //   keeps for rounding the dynamic base up to 1024 bytes; this kernel needs the
 //   base aligned already, checks it, and stops with MLA_ERR_DEVICE otherwise.
@@ -76,12 +84,18 @@ constexpr uint64_t kDrainLimitNsU = 200000000ull;
 constexpr float kLog2eU = 1.4426950408889634f;
 constexpr uint32_t kIdescPV = umma::idesc_e4m3(128, 32, 1, 1);
 constexpr uint32_t kLayoutSw64 = 4;
+constexpr uint32_t kLayoutSw32 = 6;
+// Row instance: the rope part of a tile as two halves of 32 bytes per row (4 KB each, 32-byte
+// swizzle). Block A of latent slot s (rope_addr + s kHalf) takes the first half with the latent
+// part, then the tile's P; block B (rope_addr + 3 kHalf) takes the second half of one tile at a time.
+constexpr int kHalf = kRowsU * 32;
 
 enum : int {
   kBFull = 0,     // [3] latent part of a tile landed, and the rope part in the paged instance (TMA tx, and
                   //     every loader lane's cp.async arrival)
   kBLEmpty = 3,   // [3] latent slot free (P.V done)
-  kBREmpty = 6,   // [2] rope slot free (the tile's P.V done: the slot held its P)
+  kBREmpty = 6,   // [2] rope slot free (the tile's P.V done: the slot held its P); row instance: [0] block B
+                  //     free (the tile's scores done)
   kBSFull = 8,    // [2] S^T ready
   kBPFull = 10,   // [2] P^T written into the rope slot (128 arrivals)
   kBPEmpty = 12,  // [2] P^T consumed (P.V done)
@@ -89,7 +103,8 @@ enum : int {
   kBQEmpty = 15,  // query consumed (last scores of the item done)
   kBOEmpty = 16,  // [2] O^T read by the epilogue (128 arrivals)
   kBDrain = 18,   // every MMA of the CTA done (both issuing threads commit)
-  kBRFull = 19,   // [2] rope part of a tile landed, row instance (TMA tx, and every loader lane's arrival)
+  kBRFull = 19,   // row instance: [0] the second rope half of a tile landed in block B (TMA tx, and every
+                  //     loader lane's arrival)
   kNumBars = 21
 };
 
@@ -119,6 +134,7 @@ struct SU {
 static_assert(SU::kAlloc <= 232448, "a16w8 tcgen05 stage-1 shared memory");
 static_assert(SU::kQ % 1024 == 0 && SU::kRope % 1024 == 0 && SU::kBar % 8 == 0, "operand alignment");
 static_assert(kPBuf <= kRopeStage, "a tile's P fits in its rope slot");
+static_assert(kPBuf <= kHalf && 4 * kHalf <= kRopeStages * kRopeStage, "row instance: three A blocks and B");
 
 __device__ __forceinline__ void record_error_u(int* err, int code) { atomicCAS(err, 0, code); }
 
@@ -265,6 +281,7 @@ __device__ __forceinline__ void split4_e4m3(uint32_t bf_lo, uint32_t bf_hi, floa
 
 struct KvMaps {
   CUtensorMap lat_tile, rope_tile;  // 128-row boxes
+  CUtensorMap rope_half;            // 128-row boxes of 32 rope bytes (row instance)
   CUtensorMap lat_page, rope_page;  // one-page boxes (page sizes 16..64), else unused
 };
 
@@ -369,23 +386,33 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       umma::mma_f8f6f4(d, umma::smem_desc(lat + kb * kBlk + ko, 16, 1024, umma::kLayoutSw128),
                        umma::smem_desc(q_addr + kb * kQKBlk + ko, 16, 1024, umma::kLayoutSw128), kIdescQK, st > 0);
     }
+    if constexpr (kSplit)  // the first rope half landed with the latent part, in block A of the slot
+      umma::mma_f8f6f4(d, umma::smem_desc(rope_addr + (uint32_t)(i % kLatStages) * kHalf, 16, 256, kLayoutSw32),
+                       umma::smem_desc(q_addr + kQLat, 16, 512, kLayoutSw64), kIdescQK, 1u);
   };
   auto issue_qk_rope = [&](const TCur& c, int i) {
-    const uint32_t rope = rope_addr + (i & 1) * kRopeStage;
     const uint32_t d = tmem + kColS + (uint32_t)kNQ * (uint32_t)(i & 1);
     umma::fence_after_sync();
     if (row_copy[i % kLatStages]) umma::fence_proxy_async_smem();
+    if constexpr (kSplit) {  // the second rope half, in block B
+      umma::mma_f8f6f4(d, umma::smem_desc(rope_addr + 3u * kHalf, 16, 256, kLayoutSw32),
+                       umma::smem_desc(q_addr + kQLat + 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
+    } else {
+      const uint32_t rope = rope_addr + (i & 1) * kRopeStage;
 #pragma unroll
-    for (int st = 0; st < 2; ++st)
-      umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
-                       umma::smem_desc(q_addr + kQLat + st * 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
+      for (int st = 0; st < 2; ++st)
+        umma::mma_f8f6f4(d, umma::smem_desc(rope + st * 32, 16, 512, kLayoutSw64),
+                         umma::smem_desc(q_addr + kQLat + st * 32, 16, 512, kLayoutSw64), kIdescQK, 1u);
+    }
     umma::commit(bar(kBSFull + (i & 1)));  // the rope slot frees only after the tile's P.V (it takes P)
+    if (kSplit) umma::commit(bar(kBREmpty));  // block B is free for the next tile's second half
     if (c.t0 + kRowsU >= c.t_end) umma::commit(bar(kBQEmpty));
   };
   auto issue_pv = [&](const TCur& d, int i) {
     const bool first = d.t0 == d.t_begin;
     // P^T of tile i sits in tile i's rope slot
-    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage, p0 = rope_addr + (i & 1) * kRopeStage;
+    const uint32_t lat = lat_addr + (i % kLatStages) * kLatStage;
+    const uint32_t p0 = kSplit ? rope_addr + (uint32_t)(i % kLatStages) * kHalf : rope_addr + (i & 1) * kRopeStage;
     const uint32_t ob = tmem + kColO + 128u * (uint32_t)(d.k & 1);
     umma::fence_after_sync();
     // B = [P_hi^T | P_lo^T], MN-major without swizzle: 8-token core matrices 128 B apart
@@ -398,8 +425,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                          umma::smem_desc(p0 + j * 512, 128, kPLo, umma::kLayoutNone), kIdescPV,
                          (first && j == 0) ? 0u : 1u);
     umma::commit(bar(kBPEmpty + (i & 1)));
-    umma::commit(bar(kBREmpty + (i & 1)));
-    umma::commit(bar(kBLEmpty + i % kLatStages));
+    if (!kSplit) umma::commit(bar(kBREmpty + (i & 1)));
+    umma::commit(bar(kBLEmpty + i % kLatStages));  // row instance: the latent slot and its block A
   };
 
   if (warp == 4 || warp == 7) {
@@ -414,7 +441,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int g = main_loader ? 0 : 1;  // loader rank
     if (main_loader && lane == 0) {
       umma::tma_prefetch_desc(&tm.lat_tile);
-      umma::tma_prefetch_desc(&tm.rope_tile);
+      umma::tma_prefetch_desc(kSplit ? &tm.rope_half : &tm.rope_tile);
       if (kPaged && page_boxes(a.page_size)) {
         umma::tma_prefetch_desc(&tm.lat_page);
         umma::tma_prefetch_desc(&tm.rope_page);
@@ -464,31 +491,40 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int run_ps = (kPaged && page_boxes(a.page_size)) ? a.page_size : 0;
     int nruns = 0, run_y = oob_row;
     IdleClock idle;
-    // Row instance (kSplit): a tile of consecutive rows has its latent part
-    // issued once its latent slot is free, and its rope part, on its own barrier,
-    // once its rope slot is free too. That slot holds the P of the tile two before
-    // until its P.V is done, later than the latent slot frees, and the scores over
-    // the latent dims need not wait for it. The main loader keeps at most one
-    // tile's rope part pending. Tiles copied row by row take both slots at once.
-    // The paged instance loads both parts together on one barrier: split, it
-    // measured slower.
-    auto issue_rope = [&](int t, int y) {  // main loader, whole warp
-      const uint32_t rb = bar(kBRFull + (t & 1)), rope = rope_addr + (t & 1) * kRopeStage;
+    // Row instance (kSplit): a tile's latent part and first rope half (block A of
+    // its latent slot) are loaded once the latent slot is free, onto the tile's
+    // full barrier; its second rope half goes into block B, onto a barrier of its
+    // own, once the scores of the tile before are done. The scores over the latent
+    // dims and the first half need not wait for it. The main loader keeps at most
+    // one tile's second half pending. A tile copied row by row is copied the same
+    // way: latent rows and first halves at once by both loaders, second halves by
+    // the extra loader once block B is free. The paged instance loads a tile's
+    // latent and rope parts together into a latent slot and a rope slot, on one
+    // barrier: split, it measured slower.
+    // main loader, whole warp, once block B is free: the second rope half of a box tile by TMA, or
+    // (rc: a row-copied tile, whose second half the helper copies) the arrival alone
+    auto issue_rope = [&](int t, int y, bool rc) {
+      (void)t;
+      const uint32_t rb = bar(kBRFull);
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(rb, kRopeStage);
-        umma::tma_load_2d(rope, &tm.rope_tile, 512, y, rb, pol);
+        if (rc) {
+          umma::mbar_arrive(rb);
+        } else {
+          ptx::mbar_arrive_expect_tx(rb, kHalf);
+          umma::tma_load_2d(rope_addr + 3u * kHalf, &tm.rope_half, 544, y, rb, pol);
+        }
       }
       umma::cp_async_arrive_noinc(rb);
     };
-    bool pend = false;
+    bool pend = false, pend_rc = false;
     int pend_i = 0, pend_y = oob_row;
     while (!c.done || pend) {
       bool progress = false;
       if (pend) {  // main loader of the row instance only
-        bool rfree = pend_i < 2 || ptx::mbar_test_wait(bar(kBREmpty + (pend_i & 1)), ((pend_i >> 1) - 1) & 1);
+        bool rfree = pend_i < 1 || ptx::mbar_test_wait(bar(kBREmpty), (pend_i - 1) & 1);
         rfree = __shfl_sync(~0u, rfree, 0);
         if (rfree) {
-          issue_rope(pend_i, pend_y);
+          issue_rope(pend_i, pend_y, pend_rc);
           pend = false;
           progress = true;
         }
@@ -528,14 +564,16 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (main_loader) {  // polls
           ready = i < kLatStages || ptx::mbar_test_wait(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1);
           // the rope slot is free once P.V of the tile two before is done
-          rope_ready = i < 2 || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1);
-          if (!kSplit || !cont) ready = ready && rope_ready;
+          // row instance: block B is free once the previous tile's scores are done
+          rope_ready = kSplit ? (i < 1 || ptx::mbar_test_wait(bar(kBREmpty), (i - 1) & 1))
+                              : (i < 2 || ptx::mbar_test_wait(bar(kBREmpty + rs), ((i >> 1) - 1) & 1));
+          if (!kSplit) ready = ready && rope_ready;
           ready = __shfl_sync(~0u, ready, 0);
           rope_ready = __shfl_sync(~0u, rope_ready, 0);
         } else {  // the extra loaders have nothing else to do: a bounded blocking wait
           const bool w_ok =
               (i < kLatStages || wait_u(bar(kBLEmpty + ls), ((i / kLatStages) - 1) & 1, abort_flag)) &&
-              ((kSplit && cont) || i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag));
+              (kSplit || i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag));
           if (!__all_sync(~0u, w_ok)) {
             ok = false;
             break;
@@ -543,8 +581,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           ready = true;
         }
         if (ready) {
-          const uint32_t fb = bar(kBFull + ls), rb = bar(kBRFull + rs);
-          const uint32_t lat = lat_addr + ls * kLatStage, rope = rope_addr + rs * kRopeStage;
+          const uint32_t fb = bar(kBFull + ls), rb = bar(kBRFull);
+          const uint32_t lat = lat_addr + ls * kLatStage;
+          // paged instance: the tile's rope slot; row instance: block A of the latent slot (block B is
+          // rope_addr + 3 kHalf)
+          const uint32_t rope = kSplit ? rope_addr + (uint32_t)ls * kHalf : rope_addr + rs * kRopeStage;
           if (main_loader && lane == 0) row_copy[ls] = row_copied ? 1 : 0;  // published by the arrivals below
           if (runs) {  // the paged instance only: both parts on the latent barrier
             if (main_loader) {
@@ -559,10 +600,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
           } else if (cont) {
             if (main_loader) {
-              if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kSplit ? kLatStage : kLatStage + kRopeStage);
+              if (lane == 0) ptx::mbar_arrive_expect_tx(fb, kSplit ? kLatStage + kHalf : kLatStage + kRopeStage);
               __syncwarp();
               if (lane < 4) umma::tma_load_2d(lat + lane * kBlk, &tm.lat_tile, lane * 128, y0, fb, pol);
-              if (!kSplit && lane == 4) umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
+              if (lane == 4) {
+                if (kSplit)
+                  umma::tma_load_2d(rope, &tm.rope_half, 512, y0, fb, pol);
+                else
+                  umma::tma_load_2d(rope, &tm.rope_tile, 512, y0, fb, pol);
+              }
             }
           } else {
             // Row r's index sits in lane (r & 31), slot (r >> 5); loader g of n copies the
@@ -583,38 +629,61 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                 umma::cp_async_16(dst, kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 16 * lane, valid ? 16u : 0u, pol);
               }
             }
+            if constexpr (kSplit) {
+              // the first 32 rope bytes into block A: 16 rows per instruction, lane l copies
+              // chunk l % 2 of row 16 k + l / 2 (32-byte swizzle: chunk c ^ ((r / 4) % 2))
 #pragma unroll
-            for (int i8 = 0; i8 < 16; ++i8) {
-              if (i8 % kLoaders != g) continue;
-              const int r = 8 * i8 + (lane >> 2);
-              const int yr = __shfl_sync(~0u, y0s[i8 >> 2], r & 31);
-              const bool valid = yr != oob_row;
-              const uint32_t dst = rope + r * 64 + ((((uint32_t)lane & 3u) ^ ((r >> 1) & 3)) << 4);
-              umma::cp_async_16(dst, kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 512 + 16 * (lane & 3),
-                                valid ? 16u : 0u, pol);
+              for (int k = 0; k < 8; ++k) {
+                if (k % kLoaders != g) continue;
+                const int r = 16 * k + (lane >> 1);
+                const int yr = __shfl_sync(~0u, y0s[k >> 1], r & 31);
+                const bool valid = yr != oob_row;
+                const uint32_t c2 = (uint32_t)lane & 1u;
+                umma::cp_async_16(rope + r * 32 + ((c2 ^ ((r >> 2) & 1)) << 4),
+                                  kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 512 + 16 * c2, valid ? 16u : 0u, pol);
+              }
+            } else {
+#pragma unroll
+              for (int i8 = 0; i8 < 16; ++i8) {
+                if (i8 % kLoaders != g) continue;
+                const int r = 8 * i8 + (lane >> 2);
+                const int yr = __shfl_sync(~0u, y0s[i8 >> 2], r & 31);
+                const bool valid = yr != oob_row;
+                const uint32_t dst = rope + r * 64 + ((((uint32_t)lane & 3u) ^ ((r >> 1) & 3)) << 4);
+                umma::cp_async_16(dst, kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 512 + 16 * (lane & 3),
+                                  valid ? 16u : 0u, pol);
+              }
             }
-            if (main_loader && lane == 0) {
-              umma::mbar_arrive(fb);
-              if (kSplit) umma::mbar_arrive(rb);
-            }
+            if (main_loader && lane == 0) umma::mbar_arrive(fb);
           }
           umma::cp_async_arrive_noinc(fb);
-          if constexpr (kSplit) {
-            if (row_copied) {
-              umma::cp_async_arrive_noinc(rb);
-            } else if (main_loader) {
+          if constexpr (kSplit) {  // the second rope half, once block B is free
+            if (main_loader) {
               if (rope_ready) {
-                issue_rope(i, y0);
+                issue_rope(i, y0, row_copied);
               } else {
                 pend = true;
                 pend_i = i;
                 pend_y = y0;
+                pend_rc = row_copied;
               }
-            } else {  // the extra loader arrives on the rope barrier once the rope slot is free
-              const bool r_ok = i < 2 || wait_u(bar(kBREmpty + rs), ((i >> 1) - 1) & 1, abort_flag);
+            } else {  // the extra loader: waits for block B, copies a row-copied tile's second halves
+              const bool r_ok = i < 1 || wait_u(bar(kBREmpty), (i - 1) & 1, abort_flag);
               if (!__all_sync(~0u, r_ok)) {
                 ok = false;
                 break;
+              }
+              if (row_copied) {
+                const uint8_t* kv8 = static_cast<const uint8_t*>(a.kv);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const int r = 16 * k + (lane >> 1);
+                  const int yr = __shfl_sync(~0u, y0s[k >> 1], r & 31);
+                  const bool valid = yr != oob_row;
+                  const uint32_t c2 = (uint32_t)lane & 1u;
+                  umma::cp_async_16(rope_addr + 3u * kHalf + r * 32 + ((c2 ^ ((r >> 2) & 1)) << 4),
+                                    kv8 + (valid ? (int64_t)yr * kQkDim : 0) + 544 + 16 * c2, valid ? 16u : 0u, pol);
+                }
               }
               umma::cp_async_arrive_noinc(rb);
             }
@@ -647,9 +716,9 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       if (ptx::mbar_try_wait(b_, par)) continue;
       (void)ptx::mbar_wait_bounded(b_, par, kDrainLimitNsU);
     }
-    for (int t = (i >= 2 ? i - 2 : 0); kSplit && main_loader && t < i; ++t) {
-      const uint32_t b_ = bar(kBRFull + (t & 1));
-      const uint32_t par = (uint32_t)(t >> 1) & 1u;
+    for (int t = (i >= 1 ? i - 1 : 0); kSplit && main_loader && t < i; ++t) {
+      const uint32_t b_ = bar(kBRFull);
+      const uint32_t par = (uint32_t)t & 1u;
       if (ptx::mbar_try_wait(b_, par)) continue;
       (void)ptx::mbar_wait_bounded(b_, par, kDrainLimitNsU);
     }
@@ -669,7 +738,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (!ok) break;
         issue_qk_lat(nq);
         if constexpr (kSplit) {  // the rope part has its own barrier
-          ok = wait_u(bar(kBRFull + (nq & 1)), (nq >> 1) & 1, abort_flag);
+          ok = wait_u(bar(kBRFull), nq & 1, abort_flag);
           if (!ok) break;
         }
         issue_qk_rope(c, nq);
@@ -899,9 +968,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
         // P goes into this tile's rope slot: its scores are done (S was full), and
         // the P.V two tiles before, which used the slot last, has landed
-        if (ok && i >= 2) ok = wait_u(bar(kBPEmpty + (i & 1)), ((i >> 1) - 1) & 1, abort_flag);
+        // (row instance: block A of the tile's latent slot, whose first rope half the scores have read;
+        // the P it held last, three tiles before, was read by a P.V that freed the latent slot)
+        if (!kSplit && ok && i >= 2) ok = wait_u(bar(kBPEmpty + (i & 1)), ((i >> 1) - 1) & 1, abort_flag);
         if (ok) {
-          uint8_t* pb = smem + SU::kRope + (i & 1) * kRopeStage + row * 16;
+          uint8_t* pb = smem + SU::kRope + (kSplit ? (i % kLatStages) * kHalf : (i & 1) * kRopeStage) + row * 16;
           *reinterpret_cast<uint4*>(pb) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(pb + kPLo) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
         }
@@ -1010,8 +1081,9 @@ int make_kv_maps(const void* kv, int64_t rows, int page_size, KvMaps* m) {
     cuuint32_t w, h;
     CUtensorMapSwizzle sw;
   };
-  const View views[4] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
+  const View views[5] = {{&m->lat_tile, 128, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_128B},
                          {&m->rope_tile, 64, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_64B},
+                         {&m->rope_half, 32, (cuuint32_t)kRowsU, CU_TENSOR_MAP_SWIZZLE_32B},
                          {&m->lat_page, 128, (cuuint32_t)page_size, CU_TENSOR_MAP_SWIZZLE_128B},
                          {&m->rope_page, 64, (cuuint32_t)page_size, CU_TENSOR_MAP_SWIZZLE_64B}};
   *m = KvMaps{};

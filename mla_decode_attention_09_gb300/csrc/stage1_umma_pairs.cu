@@ -21,7 +21,7 @@
 // double-buffered O measured 89.7 against 84.2 us for two tokens, B = 64,
 // kv_len = 8192.)
 //
-// The layout of shared memory is that of the a16w8 kernel (stage1_umma_a16.cu):
+// The layout of shared memory is that of the a16w8 kernel's paged instance (stage1_umma_a16.cu):
 // the staged query is 18 KB, and a tile's P (8 KB: two terms for two tokens)
 // lives in that tile's rope slot, whose rope bytes are dead once the tile's
 // scores are done. Only two tiles are then in flight: a tile's rope part waits
