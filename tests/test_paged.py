@@ -143,3 +143,20 @@ def test_paged_full_size(mla, order):
     assert plan.check_error() == 0
     # every sequence, element by element
     compare(out, oracle_paged(inp), mi.MODE_FP8, f"paged full size {order}")
+
+
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("ps", [16, 64])
+def test_half_shuffled_pages(mla, mode, k8, ps):
+    """Page order kept for half of the pages and shuffled for the rest: tiles inside runs of pages
+    in order load as one box, the others as page boxes (or row copies where a page is out of step)."""
+    lengths = [1500, 700, 2000, 130]
+    inp = mi.make_paged_inputs(lengths, ps, mode, seed=77, extra_pages=3)
+    ix = inp.kv_indices.clone()
+    g = torch.Generator().manual_seed(5)
+    n = ix.numel()
+    pick = torch.nonzero(torch.rand(n, generator=g) < 0.5).flatten()
+    ix[pick] = ix[pick][torch.randperm(pick.numel(), generator=g)]
+    inp.kv_indices = ix
+    out, _ = run_paged(mla, inp, **k8)
+    compare(out, oracle_paged(inp), mode, f"half-shuffled pages of {ps}")

@@ -86,6 +86,37 @@ def test_odd_lengths(mla, mode, k8, split):
     compare(out, oracle_out(inp), mode, f"odd lengths {split}")
 
 
+def mixed_tile_inputs(mode: int) -> mi.Inputs:
+    """Rows in order, except that every third 128-row chunk of a sequence has its rows shuffled among
+    themselves, and the chunk after it has one row moved to a spare slot: box-loaded tiles and
+    row-copied tiles alternate within each sequence."""
+    lengths = [1500, 700, 2000, 130, 5]
+    inp = mi.make_inputs(lengths, mode, seed=321, extra_slots=5)
+    ix = inp.kv_indices.clone()
+    g = torch.Generator().manual_seed(9)
+    ip = inp.kv_indptr.tolist()
+    for b in range(len(lengths)):
+        for k, t0 in enumerate(range(ip[b], ip[b + 1], 128)):
+            t1 = min(t0 + 128, ip[b + 1])
+            if k % 3 == 1:
+                ix[t0:t1] = ix[t0:t1][torch.randperm(t1 - t0, generator=g)]
+            elif k % 3 == 2 and t1 - t0 > 1:
+                ix[t0 + (t1 - t0) // 2] = inp.kv.shape[0] - 1 - (k % 5)
+    inp.kv_indices = ix
+    return inp
+
+
+@pytest.mark.parametrize("mode,k8", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("split", ["whole", "split"])
+def test_mixed_box_and_row_copied_tiles(mla, mode, k8, split):
+    inp = mixed_tile_inputs(mode)
+    opts = {} if split == "whole" else {"min_rows_per_split": 64}
+    out, plan = run(mla, inp, num_sms=152 if split == "whole" else 7, **k8, **opts)
+    if split == "split":
+        assert plan.info()["num_split_seqs"] > 0
+    compare(out, oracle_out(inp), mode, f"mixed tiles {split}")
+
+
 @pytest.mark.parametrize("k8", [{}, {"fp8_kernel": 1}], ids=["a16w8-tcgen05", "a16w8-mma"])
 @pytest.mark.parametrize("q_std", [1.0, 2.0])
 def test_a16w8_keeps_the_bf16_query(mla, k8, q_std):
